@@ -1,0 +1,388 @@
+#!/usr/bin/env python3
+"""Benchmark of exact multi-head attention (forward + backward) on GB300.
+
+One step = the whole path over one batch: attn_fwd (O, LSE), then the three backward phases
+(attn_bwd_preprocess, attn_bwd_main, attn_bwd_dq_convert), all through the C ABI on device-
+resident inputs.  Default workload: the long-text sequence, B=2, H=16, N=16384, d_k=128, bf16,
+Q and K ~ N(0, 2^2), V and dO ~ N(0, 1), scale 1/sqrt(128).  The metric counts
+4*B*H*N^2*d_k flops for the forward and 10*B*H*N^2*d_k for the backward.
+
+Prints ONE JSON line (rank 0).  Under torchrun each rank runs its own batch on its own GPU
+(independent problems; no data-path collective), `value` is the total over ranks divided by
+the slowest rank's time.
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same workload (one head,
+its first --oracle-tokens tokens), the only other place this script runs the oracle.
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd/bwd TFLOPS (4·BHN²d / 10·BHN²d) and % of GB300 bf16 peak"
+UNIT = "TFLOPS"
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "bwd_main_long_text.md")
+KERNEL_SOURCES = [os.path.join(ROOT, "self_attention_gb300", "csrc", f)
+                  for f in ("attn_bwd.cu", "common.cuh", "ptx.cuh")]
+# Peaks used when the measured-peaks file is absent (one earlier GB300 measurement).
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=60)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="long_text")
+    p.add_argument("--shape", default=None,
+                   help="B,H,N,d override of the workload's sizes (profiling small cases)")
+    p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--oracle-tokens", type=int, default=2048,
+                   help="tokens of one head the CPU oracle runs on per reference-arm step")
+    p.add_argument("--cpu-baseline-tokens", type=int, default=8192,
+                   help="tokens of one head the CPU oracle runs on for cpu_baseline (~10-30 s)")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args(argv)
+
+
+def workload(args):
+    from self_attention_gb300.inputs import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.shape:
+        B, H, N, d = (int(x) for x in args.shape.split(","))
+        w = dataclasses.replace(w, name=f"{w.name}_{B}x{H}x{N}x{d}", B=B, H=H, N=N, d=d)
+    return w
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_over_ranks(local: dict, world: int) -> dict:
+    """MAX of every '*_ms' entry and SUM of every other numeric entry over the ranks (a single
+    all_reduce of a small tensor per operation; nothing else crosses ranks)."""
+    if world == 1:
+        return dict(local)
+    import torch
+    import torch.distributed as dist
+    keys = sorted(local)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    mx = torch.tensor([float(local[k]) if k.endswith("_ms") else 0.0 for k in keys],
+                      dtype=torch.float64, device=dev)
+    sm = torch.tensor([0.0 if k.endswith("_ms") else float(local[k]) for k in keys],
+                      dtype=torch.float64, device=dev)
+    dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+    dist.all_reduce(sm, op=dist.ReduceOp.SUM)
+    return {k: (mx[i] if k.endswith("_ms") else sm[i]).item() for i, k in enumerate(keys)}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {k: float(pk[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(units_per_launch: float):
+    """DRAM bytes per launch of the backward main kernel from the committed ncu summary,
+    scaled from the profiled case by the units (query x key tile pairs) a launch processes;
+    None if the kernel source changed since the counters were taken."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
+    m_bytes = re.search(r"dram_bytes_per_unit:\s*([0-9.eE+]+)", text)
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+        return None
+    return float(m_bytes.group(1)) * units_per_launch
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", gpu_id], stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        self.proc.terminate()
+        self.proc.wait()
+        self.file.seek(0)
+        sm, mx, reasons = [], [], set()
+        for line in self.file.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(self.NAMES, parts[3:7]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        self.file.close()
+        os.unlink(self.file.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def oracle_sample(w, tokens: int):
+    """One head (b=0, h=0) of the workload, its first `tokens` tokens (same distribution)."""
+    from self_attention_gb300.inputs import make_workload_inputs
+    s = min(tokens, w.N)
+    small = dataclasses.replace(w, B=1, H=1, N=s) if not w.model_dim else w
+    inp = make_workload_inputs(small)
+    sl = lambda t: t[:1, :1, :s].contiguous()
+    return {x: sl(inp[x]) for x in ("q", "k", "v", "do")}, s
+
+
+def time_oracle(w, tokens: int, repeats: int):
+    import oracle
+    sample, s = oracle_sample(w, tokens)
+    oracle.build()
+    times = []
+    for _ in range(repeats):
+        t0 = time.perf_counter()
+        oracle.fwd(sample["q"], sample["k"], sample["v"], w.scale)
+        oracle.bwd(sample["q"], sample["k"], sample["v"], sample["do"], w.scale)
+        times.append(time.perf_counter() - t0)
+    flops = 14.0 * s * s * w.d
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    desc = (f"oracle fwd+bwd (fp64, N x N materialised) on one head of {w.name}: its first {s} "
+            f"tokens, d_k={w.d}; {14 * s * s * w.d:.3g} metric flops per run")
+    return times, flops, cores, desc
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    w = workload(args)
+    for _ in range(args.warmup):
+        time_oracle(w, args.oracle_tokens, 1)
+    times, flops, cores, desc = time_oracle(w, args.oracle_tokens, args.steps)
+    per_step = sum(times) / len(times)
+    value = flops / per_step / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d_k": w.d,
+                   "seq_len": w.N, "global_batch": w.B},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    import torch.distributed as dist
+
+    import self_attention_gb300 as sa
+    from self_attention_gb300.build import build
+    from self_attention_gb300.inputs import make_workload_inputs
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    sa.load_library(build())
+    w = workload(args)
+    B, H, N, D, scale = w.B, w.H, w.N, w.d, w.scale
+    inp = make_workload_inputs(dataclasses.replace(w, seed=w.seed + 7919 * rank))
+    host = {x: inp[x].pin_memory() for x in ("q", "k", "v", "do")}
+    q, k, v, do = (host[x].cuda() for x in ("q", "k", "v", "do"))
+    o, dq, dk, dv = (torch.empty_like(q) for _ in range(4))
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    ws_bytes = sa.attn_bwd_workspace_size(B, H, N, D)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        sa.attn_fwd(q, k, v, o, lse, B, H, N, D, scale, stream)
+        if ev:
+            ev[1].record(stream)
+        sa.attn_bwd_preprocess(o, do, ws, ws_bytes, B, H, N, D, stream)
+        if ev:
+            ev[2].record(stream)
+        sa.attn_bwd_main(q, k, v, do, lse, dk, dv, ws, ws_bytes, B, H, N, D, scale, stream)
+        if ev:
+            ev[3].record(stream)
+        sa.attn_bwd_dq_convert(ws, ws_bytes, dq, B, H, N, D, scale, stream)
+        if ev:
+            ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if sa.attn_get_device_status() != 0:
+        raise RuntimeError("device status reported a kernel timeout during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    props = torch.cuda.get_device_properties(local)
+    gpu_id = str(getattr(props, "uuid", local))
+    gpu_id = gpu_id if gpu_id.startswith("GPU-") or gpu_id.isdigit() else f"GPU-{gpu_id}"
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(gpu_id)
+    time.sleep(0.3)
+    start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    stop.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if world > 1:
+        dist.barrier()
+    if sa.attn_get_device_status() != 0:
+        raise RuntimeError("device status reported a kernel timeout in the timed region")
+
+    ms = lambda a, b: a.elapsed_time(b)
+    local_res = {
+        "step_ms": ms(start, stop) / args.steps,
+        "fwd_ms": statistics.mean(ms(e[0], e[1]) for e in evs),
+        "bwd_ms": statistics.mean(ms(e[1], e[4]) for e in evs),
+        "bwd_main_ms": statistics.mean(ms(e[2], e[3]) for e in evs),
+        "flops": (4.0 + 10.0) * B * H * N * N * D,
+    }
+
+    # end to end through the public API: pinned host inputs -> device, forward, backward,
+    # outputs back to pinned host buffers, all inside the timed region
+    out_host = {x: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                for x, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+    dev_in = {x: torch.empty_like(host[x], device="cuda") for x in host}
+
+    def e2e_step():
+        for x in host:
+            dev_in[x].copy_(host[x], non_blocking=True)
+        oo, ll = sa.forward(dev_in["q"], dev_in["k"], dev_in["v"], scale)
+        g = sa.backward(dev_in["q"], dev_in["k"], dev_in["v"], oo, dev_in["do"], ll, scale,
+                        workspace=ws)
+        for x, t in zip(("o", "lse", "dq", "dk", "dv"), (oo, ll, *g)):
+            out_host[x].copy_(t, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    local_res["e2e_ms"] = e0.elapsed_time(e1) / args.e2e_steps
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in out_host.values())
+
+    res = reduce_over_ranks(local_res, world)
+    if rank != 0:
+        dist.destroy_process_group()
+        return 0
+
+    peaks, peak_src = load_peaks()
+    flops_total = res["flops"]
+    value = flops_total / (res["step_ms"] * 1e-3) / 1e12
+    per_gpu_fwd = 4.0 * B * H * N * N * D / (local_res["fwd_ms"] * 1e-3) / 1e12
+    per_gpu_bwd = 10.0 * B * H * N * N * D / (local_res["bwd_ms"] * 1e-3) / 1e12
+    main_flops = 10.0 * B * H * N * N * D
+    achieved = main_flops / (local_res["bwd_main_ms"] * 1e-3) / 1e12
+    peak = peaks["bf16_tflops_sustained"]
+    units = B * H * math.ceil(N / 128) * math.ceil(N / 64)   # (key tile, query tile) pairs
+    traffic = profiled_traffic(units)
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        times, oflops, cores, desc = time_oracle(w, args.cpu_baseline_tokens, 1)
+        cpu = {"value": oflops / times[0] / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": desc + f"; wall {times[0]:.2f} s"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": res["step_ms"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": B, "H": H, "N": N, "d_k": D, "seq_len": N,
+                   "global_batch": B * world, "parallelism": f"independent batches x{world}",
+                   "qk_std": w.qk_std, "l2": "no flush: inputs (Q,K,V,dO = "
+                   f"{h2d / 1e6:.0f} MB) are larger than the 129 MB L2"},
+        "fwd_tflops": per_gpu_fwd, "bwd_tflops": per_gpu_bwd,
+        "fwd_pct_of_bf16_peak": 100.0 * per_gpu_fwd / peaks["bf16_tflops"],
+        "bwd_pct_of_bf16_peak": 100.0 * per_gpu_bwd / peaks["bf16_tflops"],
+        "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback",
+        "roofline": {"kernel": "bwd_main_kernel<128>" if D == 128 else "bwd_main_kernel<64>",
+                     "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "note": f"peak = {peak_src} sustained dense bf16; achieved = 10*B*H*N^2*d "
+                             "flops per launch / CUDA-event launch time"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": flops_total / (res["e2e_ms"] * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

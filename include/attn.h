@@ -1,0 +1,141 @@
+/*
+ * attn.h: C ABI of the GB300 (sm_103a) exact multi-head attention library.
+ *
+ * The operation comes from "Self-attention, CUDA kernels and FlashAttention" (2026-11-15):
+ *   section 1 "How self-attention works mathematically in a Vision Transformer":
+ *       Scores = Q K^T / sqrt(d_k); a softmax along each row (each row sums to one);
+ *       Attention(Q, K, V) = softmax(Q K^T / sqrt(d_k)) V; the same computation runs
+ *       independently for every head.
+ *   section 3 "FlashAttention: solving the Transformer memory bottleneck":
+ *       tiled, fused evaluation that never stores the N x N matrix in HBM ("Tiling"), an
+ *       online softmax ("The online softmax trick"), and a backward pass that keeps only
+ *       small per-row normalisation statistics and recomputes the attention tiles on chip
+ *       ("Recomputation in backpropagation").
+ *
+ * Conventions shared by every entry point:
+ *   - Tensors are dense, contiguous, row-major [B, H, N, d_k] bf16 (`const void *` / `void *`
+ *     here, so that the header needs no CUDA half-precision types).  Row (b, h, i) starts at
+ *     element ((b * H + h) * N + i) * d_k.  `lse` and the other per-row vectors are [B, H, N]
+ *     fp32.  All pointers are device pointers, 16-byte aligned.
+ *   - `scale` multiplies Q K^T before the softmax; pass 1/sqrt(d_k) for the article's
+ *     formula.  It must be finite and > 0.
+ *   - Supported: d_k in {64, 128}; B, H, N >= 1; B*H*N*d_k < 2^40 elements; N < 2^31.
+ *   - Ownership: the caller allocates and owns every buffer, including the backward
+ *     workspace.  The library allocates no device memory on these paths.
+ *   - Calls enqueue work on `stream` and return without waiting; only
+ *     attn_get_device_status() synchronises (that stream).  Outputs must not overlap inputs.
+ *   - Errors: every argument check runs before any launch; on failure the call returns a
+ *     non-zero attn_status and launches nothing.  A kernel that cannot make progress does not
+ *     hang the GPU: each of its waits gives up after a bounded time and records
+ *     ATTN_ERR_TIMEOUT in a per-device status word, read by attn_get_device_status().
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,     /* null pointer, size < 1, bad scale, overlapping buffers */
+    ATTN_ERR_UNSUPPORTED_DK = 2,  /* d_k not in {64, 128} */
+    ATTN_ERR_MISALIGNED = 3,      /* a pointer not 16-byte aligned */
+    ATTN_ERR_LAUNCH = 4,          /* the CUDA runtime refused a launch or a query */
+    ATTN_ERR_TIMEOUT = 5,         /* a kernel wait gave up (reported by attn_get_device_status) */
+    ATTN_ERR_WORKSPACE = 6,       /* workspace null, misaligned or smaller than required */
+    ATTN_ERR_DEVICE = 7           /* the current device is not an sm_103 GPU */
+} attn_status;
+
+/*
+ * Forward pass (section 1's Attention(Q,K,V); section 3's tiling and online softmax).
+ *   q, k, v : [B,H,N,d_k] bf16 inputs.
+ *   o       : [B,H,N,d_k] bf16 output, O = softmax(scale * Q K^T) V, rounded to nearest.
+ *   lse     : [B,H,N] fp32 output, lse[b,h,i] = log(sum_j exp(scale * q_i . k_j)) (natural
+ *             log): the per-row statistic the backward pass recomputes the tiles from.
+ */
+attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                     int H, int N, int d_k, float scale, cudaStream_t stream);
+
+/*
+ * Bytes of device workspace attn_bwd() needs for these sizes: D = rowsum(dO o O) ([B,H,N]
+ * fp32) and an fp32 dQ accumulator ([B,H,N,d_k]), each 256-byte aligned.  Returns 0 if the
+ * sizes are unsupported.
+ */
+size_t attn_bwd_workspace_size(int B, int H, int N, int d_k);
+
+/*
+ * Backward pass (section 3, "Recomputation in backpropagation": only the per-row statistic
+ * `lse` from attn_fwd is kept; the probabilities are recomputed on chip).  With
+ * P = exp(scale * Q K^T - lse) and D_i = sum_c dO_ic O_ic:
+ *   dV = P^T dO;   dP = dO V^T;   dS = P o (dP - D);   dQ = scale * dS K;   dK = scale * dS^T Q.
+ *   q, k, v, o, dout : [B,H,N,d_k] bf16 inputs (o is attn_fwd's output, dout = dL/dO).
+ *   lse              : [B,H,N] fp32 from attn_fwd for the same q, k, scale.
+ *   dq, dk, dv       : [B,H,N,d_k] bf16 outputs.
+ *   workspace        : device memory of at least attn_bwd_workspace_size(B,H,N,d_k) bytes,
+ *                      256-byte aligned, owned by the caller; its contents on entry do not
+ *                      matter and on return are unspecified.
+ * dQ is accumulated across key tiles with fp32 atomic additions, so its low-order bits may
+ * differ from run to run; dK and dV are deterministic.
+ */
+attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
+                     const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                     void *workspace, size_t workspace_bytes, int B, int H, int N, int d_k,
+                     float scale, cudaStream_t stream);
+
+/*
+ * The three stream-ordered phases attn_bwd() runs, for callers that schedule or time them
+ * separately.  Run on one stream, in this order, with the same sizes, scale and workspace,
+ * they produce exactly what attn_bwd() produces.
+ *
+ * attn_bwd_preprocess: D_i = sum_c dO_ic O_ic into the workspace's D vector, and zeroes the
+ *   workspace's fp32 dQ accumulator.  Reads o and dout.
+ * attn_bwd_main: for every 128-key tile, recomputes P from q, k and lse, and writes dk
+ *   (= scale * dS^T Q) and dv (= P^T dO); adds dS K into the dQ accumulator.  Reads q, k, v,
+ *   dout, lse and the workspace's D vector.
+ * attn_bwd_dq_convert: dq = bf16(scale * accumulator).
+ */
+attn_status attn_bwd_preprocess(const void *o, const void *dout, void *workspace,
+                                size_t workspace_bytes, int B, int H, int N, int d_k,
+                                cudaStream_t stream);
+attn_status attn_bwd_main(const void *q, const void *k, const void *v, const void *dout,
+                          const float *lse, void *dk, void *dv, void *workspace,
+                          size_t workspace_bytes, int B, int H, int N, int d_k, float scale,
+                          cudaStream_t stream);
+attn_status attn_bwd_dq_convert(void *workspace, size_t workspace_bytes, void *dq, int B, int H,
+                                int N, int d_k, float scale, cudaStream_t stream);
+
+/*
+ * Reads and clears the current device's status word after synchronising `stream`.
+ * Returns ATTN_OK, ATTN_ERR_TIMEOUT if a kernel wait gave up since the last call, or
+ * ATTN_ERR_LAUNCH if the stream reports a CUDA error.
+ */
+attn_status attn_get_device_status(cudaStream_t stream);
+
+/* A static, human-readable name for a status code. */
+const char *attn_status_string(attn_status status);
+
+/*
+ * The CUDA call behind the most recent ATTN_ERR_LAUNCH returned on the calling host thread,
+ * with the runtime's error name and text ("no error" if there was none).  The string belongs
+ * to the library and stays valid until the thread's next failing call.
+ */
+const char *attn_last_error_string(void);
+
+/*
+ * Diagnostics: launches one tiny kernel that waits, with the library's bounded-wait
+ * routine, on a barrier nothing ever signals, giving up after `limit_us` microseconds
+ * (1 ... 10^6).  The following attn_get_device_status() must then return ATTN_ERR_TIMEOUT.
+ * Used to test the failure path without hanging or faulting the GPU.
+ */
+attn_status attn_debug_wait_timeout(unsigned limit_us, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

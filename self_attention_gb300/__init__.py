@@ -1,1 +1,223 @@
-"""GB300-native exact multi-head scaled dot-product attention (placeholder during bring-up)."""
+"""GB300-native exact multi-head scaled dot-product attention.
+
+Thin Python binding over the C ABI in include/attn.h (libattn_gb300.so, built for sm_103a by
+``self_attention_gb300.build``).  This module only marshals arguments: every step of the
+computation runs in the library's CUDA kernels.  PyTorch supplies device memory and the
+current stream.  If the library is missing or cannot be loaded, every call raises: there is
+no fallback implementation.
+
+Operation ("Self-attention, CUDA kernels and FlashAttention", section 1):
+    O = softmax(scale * Q K^T) V,  scale = 1/sqrt(d_k) by default,
+per (batch, head), with tensors laid out [B, H, N, d_k] bf16.  The forward also returns
+LSE = log sum_j exp(scale * q_i . k_j) per row ([B, H, N] fp32), the statistic the backward
+pass recomputes the attention tiles from (section 3, "Recomputation in backpropagation").
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+from .build import LIB_PATH
+
+__all__ = [
+    "AttnError", "attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess",
+    "attn_bwd_main", "attn_bwd_dq_convert", "attn_get_device_status",
+    "attn_status_string", "attn_last_error_string", "attn_debug_wait_timeout", "forward", "backward", "attention",
+    "load_library", "STATUS",
+]
+
+STATUS = {
+    0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED_DK",
+    3: "ATTN_ERR_MISALIGNED", 4: "ATTN_ERR_LAUNCH", 5: "ATTN_ERR_TIMEOUT",
+    6: "ATTN_ERR_WORKSPACE", 7: "ATTN_ERR_DEVICE",
+}
+EXPORTS = ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess",
+           "attn_bwd_main", "attn_bwd_dq_convert", "attn_get_device_status", "attn_status_string",
+           "attn_last_error_string", "attn_debug_wait_timeout")
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        msg = f"{where}: {attn_status_string(code)}"
+        if code == 4:
+            msg += f" [{attn_last_error_string()}]"
+        super().__init__(msg)
+
+
+_lib = None
+_VP, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libattn_gb300.so and declare its signatures (no GPU needed to load it)."""
+    global _lib
+    if _lib is not None and path == LIB_PATH:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"libattn_gb300.so not found at {path}: build it with "
+            "`python -c 'import __graft_entry__ as g; g.build()'` (needs nvcc)")
+    lib = ctypes.CDLL(path)
+    lib.attn_fwd.argtypes = [_VP] * 5 + [_I] * 4 + [_F, _VP]
+    lib.attn_fwd.restype = _I
+    lib.attn_bwd_workspace_size.argtypes = [_I] * 4
+    lib.attn_bwd_workspace_size.restype = _SZ
+    lib.attn_bwd.argtypes = [_VP] * 10 + [_SZ] + [_I] * 4 + [_F, _VP]
+    lib.attn_bwd.restype = _I
+    lib.attn_bwd_preprocess.argtypes = [_VP] * 3 + [_SZ] + [_I] * 4 + [_VP]
+    lib.attn_bwd_preprocess.restype = _I
+    lib.attn_bwd_main.argtypes = [_VP] * 8 + [_SZ] + [_I] * 4 + [_F, _VP]
+    lib.attn_bwd_main.restype = _I
+    lib.attn_bwd_dq_convert.argtypes = [_VP, _SZ, _VP] + [_I] * 4 + [_F, _VP]
+    lib.attn_bwd_dq_convert.restype = _I
+    lib.attn_get_device_status.argtypes = [_VP]
+    lib.attn_get_device_status.restype = _I
+    lib.attn_status_string.argtypes = [_I]
+    lib.attn_status_string.restype = ctypes.c_char_p
+    lib.attn_last_error_string.argtypes = []
+    lib.attn_last_error_string.restype = ctypes.c_char_p
+    lib.attn_debug_wait_timeout.argtypes = [ctypes.c_uint, _VP]
+    lib.attn_debug_wait_timeout.restype = _I
+    if path == LIB_PATH:
+        _lib = lib
+    return lib
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t) -> int:
+    return t.data_ptr() if isinstance(t, torch.Tensor) else int(t)
+
+
+def _raise(code: int, where: str):
+    if code != 0:
+        raise AttnError(code, where)
+
+
+def attn_status_string(code: int) -> str:
+    try:
+        return load_library().attn_status_string(int(code)).decode()
+    except RuntimeError:
+        return STATUS.get(int(code), f"unknown status {code}")
+
+
+def attn_last_error_string() -> str:
+    return load_library().attn_last_error_string().decode()
+
+
+# ---------------------------------------------------------------- C-ABI mirrors (same names)
+def attn_fwd(q, k, v, o, lse, B: int, H: int, N: int, d_k: int, scale: float, stream=None):
+    """Enqueue the forward pass: o and lse written from q, k, v ([B,H,N,d_k] bf16 device)."""
+    _raise(load_library().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d_k,
+                                   float(scale), _stream(stream)), "attn_fwd")
+
+
+def attn_bwd_workspace_size(B: int, H: int, N: int, d_k: int) -> int:
+    return int(load_library().attn_bwd_workspace_size(B, H, N, d_k))
+
+
+def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes: int, B: int, H: int,
+             N: int, d_k: int, scale: float, stream=None):
+    """Enqueue the backward pass into dq, dk, dv (workspace: caller-owned device memory)."""
+    _raise(load_library().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
+                                   _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+                                   int(workspace_bytes), B, H, N, d_k, float(scale),
+                                   _stream(stream)), "attn_bwd")
+
+
+def attn_bwd_preprocess(o, dout, workspace, workspace_bytes: int, B: int, H: int, N: int,
+                        d_k: int, stream=None):
+    _raise(load_library().attn_bwd_preprocess(_ptr(o), _ptr(dout), _ptr(workspace),
+                                              int(workspace_bytes), B, H, N, d_k, _stream(stream)),
+           "attn_bwd_preprocess")
+
+
+def attn_bwd_main(q, k, v, dout, lse, dk, dv, workspace, workspace_bytes: int, B: int, H: int,
+                  N: int, d_k: int, scale: float, stream=None):
+    _raise(load_library().attn_bwd_main(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(lse), _ptr(dk),
+                                        _ptr(dv), _ptr(workspace), int(workspace_bytes), B, H, N,
+                                        d_k, float(scale), _stream(stream)), "attn_bwd_main")
+
+
+def attn_bwd_dq_convert(workspace, workspace_bytes: int, dq, B: int, H: int, N: int, d_k: int,
+                        scale: float, stream=None):
+    _raise(load_library().attn_bwd_dq_convert(_ptr(workspace), int(workspace_bytes), _ptr(dq), B,
+                                              H, N, d_k, float(scale), _stream(stream)),
+           "attn_bwd_dq_convert")
+
+
+def attn_get_device_status(stream=None) -> int:
+    """Synchronise the stream, then read and clear the device status word (0 = ATTN_OK)."""
+    return int(load_library().attn_get_device_status(_stream(stream)))
+
+
+def attn_debug_wait_timeout(limit_us: int, stream=None):
+    _raise(load_library().attn_debug_wait_timeout(int(limit_us), _stream(stream)),
+           "attn_debug_wait_timeout")
+
+
+# ---------------------------------------------------------------- tensor-level convenience
+def _check_inputs(*ts):
+    q = ts[0]
+    if q.dim() != 4:
+        raise ValueError("expected [B, H, N, d_k] tensors")
+    for t in ts:
+        if t.shape != q.shape or t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v (and o, dO) must be contiguous bf16 CUDA tensors of one shape")
+        if t.device != q.device:
+            raise ValueError("all tensors must be on the same device")
+    return q.shape
+
+
+def forward(q, k, v, scale: float | None = None, stream=None):
+    """Returns (o, lse): o [B,H,N,d_k] bf16, lse [B,H,N] fp32 (natural log)."""
+    B, H, N, D = _check_inputs(q, k, v)
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    attn_fwd(q, k, v, o, lse, B, H, N, D, scale, stream)
+    return o, lse
+
+
+def backward(q, k, v, o, dout, lse, scale: float | None = None, stream=None, workspace=None):
+    """Returns (dq, dk, dv) bf16 for the loss gradient dout = dL/dO."""
+    B, H, N, D = _check_inputs(q, k, v, o, dout)
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    nbytes = attn_bwd_workspace_size(B, H, N, D)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace.numel(), B, H, N, D, scale,
+             stream)
+    return dq, dk, dv
+
+
+class _Attention(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, scale):
+        o, lse = forward(q, k, v, scale)
+        ctx.save_for_backward(q, k, v, o, lse)
+        ctx.scale = scale
+        return o
+
+    @staticmethod
+    def backward(ctx, dout):
+        q, k, v, o, lse = ctx.saved_tensors
+        dq, dk, dv = backward(q, k, v, o, dout.contiguous(), lse, ctx.scale)
+        return dq, dk, dv, None
+
+
+def attention(q, k, v, scale: float | None = None):
+    """softmax(scale * Q K^T) V with autograd support."""
+    D = q.shape[-1]
+    return _Attention.apply(q, k, v, 1.0 / math.sqrt(D) if scale is None else scale)

@@ -1,0 +1,355 @@
+// The C ABI declared in include/attn.h: argument validation, TMA descriptor construction and
+// the device status word.  Compute happens only in the kernels this file launches.
+#include "attn.h"
+#include "common.cuh"
+#include "kernels.h"
+
+#include <cudaTypedefs.h>
+#include <cmath>
+#include <cstring>
+#include <cstdio>
+#include <mutex>
+
+namespace attn {
+
+// One status word per device (a __device__ variable lives in every device context).
+__device__ int g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    bool supported = false;
+    int *status = nullptr;  // device address of g_status_word on that device
+};
+
+std::mutex g_mutex;
+thread_local char t_last_error[192] = "no error";
+
+// Records a failed CUDA call for attn_last_error_string() and maps it to ATTN_ERR_LAUNCH.
+attn_status fail(const char *what, cudaError_t e)
+{
+    std::snprintf(t_last_error, sizeof t_last_error, "%s: %s (%s)", what, cudaGetErrorName(e),
+                  cudaGetErrorString(e));
+    return ATTN_ERR_LAUNCH;
+}
+DeviceState g_devices[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Resolves, once per device, whether it is an sm_103 part and where its status word is.
+attn_status device_state(DeviceState **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail("cudaGetDevice", e);
+    if (dev < 0 || dev >= kMaxDevices) return fail("cudaGetDevice", cudaErrorInvalidDevice);
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState &s = g_devices[dev];
+    if (!s.ready) {
+        int major = 0, minor = 0;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+            return fail("cudaDeviceGetAttribute", e);
+        s.supported = (major == 10 && minor == 3);
+        if (s.supported) {
+            void *p = nullptr;
+            if ((e = cudaGetSymbolAddress(&p, g_status_word)) != cudaSuccess)
+                return fail("cudaGetSymbolAddress", e);
+            s.status = static_cast<int *>(p);
+        }
+        if (!g_encode) {
+            void *fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q);
+            if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+                return fail("cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)",
+                            e != cudaSuccess ? e : cudaErrorSymbolNotFound);
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        s.ready = true;
+    }
+    if (!s.supported) return ATTN_ERR_DEVICE;
+    *out = &s;
+    return ATTN_OK;
+}
+
+// 3-D map over [BH, N, d] bf16 (innermost first: d, N, BH), boxes of 64 x box_rows x 1 with
+// the 128-byte swizzle.  Rows past N (or past a head) read as zeros.
+bool make_map(CUtensorMap *m, const void *base, int bh, int n, int d, int box_rows)
+{
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)n, (cuuint64_t)bh};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)n * d * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+    cuuint32_t elem[3] = {1, 1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+                    box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Range {
+    uintptr_t lo, hi;
+};
+
+bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+
+Range span(const void *p, size_t bytes)
+{
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    return Range{lo, lo + bytes};
+}
+
+attn_status check_sizes(int B, int H, int N, int d_k, float scale)
+{
+    if (d_k != 64 && d_k != 128) return ATTN_ERR_UNSUPPORTED_DK;
+    if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+    const long long bh = (long long)B * H;
+    if (bh > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+    if (bh * (long long)N * d_k >= (1LL << 40)) return ATTN_ERR_INVALID_ARG;
+    // one CTA per 256 query rows of a head must fit a 1-D grid
+    if (bh * (((long long)N + 255) / 256) > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+    return ATTN_OK;
+}
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                                int B, int H, int N, int d_k, float scale, cudaStream_t stream)
+{
+    attn_status st = check_sizes(B, H, N, d_k, scale);
+    if (st != ATTN_OK) return st;
+    if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return ATTN_ERR_MISALIGNED;
+    const long long bh = (long long)B * H;
+    const size_t tbytes = (size_t)bh * N * d_k * 2, lbytes = (size_t)bh * N * 4;
+    const Range ins[3] = {span(q, tbytes), span(k, tbytes), span(v, tbytes)};
+    const Range ro = span(o, tbytes), rl = span(lse, lbytes);
+    if (overlap(ro, rl)) return ATTN_ERR_INVALID_ARG;
+    for (const Range &r : ins)
+        if (overlap(r, ro) || overlap(r, rl)) return ATTN_ERR_INVALID_ARG;
+
+    DeviceState *dev = nullptr;
+    if ((st = device_state(&dev)) != ATTN_OK) return st;
+    FwdArgs a;
+    std::memset(&a, 0, sizeof a);
+    if (!make_map(&a.tm_q, q, (int)bh, N, d_k, 128) || !make_map(&a.tm_k, k, (int)bh, N, d_k, 128) ||
+        !make_map(&a.tm_v, v, (int)bh, N, d_k, 128))
+        return fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
+    a.o = o;
+    a.lse = lse;
+    a.bh = (int)bh;
+    a.n = N;
+    a.d = d_k;
+    a.scale = scale;
+    a.status = dev->status;
+    const cudaError_t e = launch_fwd(a, stream);
+    return e == cudaSuccess ? ATTN_OK : fail("attn_fwd launch", e);
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+extern "C" size_t attn_bwd_workspace_size(int B, int H, int N, int d_k)
+{
+    if (check_sizes(B, H, N, d_k, 1.0f) != ATTN_OK) return 0;
+    const size_t rows = (size_t)B * H * N;
+    return align256(rows * 4) + align256(rows * d_k * 4);
+}
+
+namespace {
+
+// Validates what a backward phase needs and fills `a`.  Null pointers mark operands the phase
+// does not use (they are neither checked nor mapped); the workspace is always required.
+attn_status prepare_bwd(BwdArgs &a, const void *q, const void *k, const void *v, const void *o,
+                        const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                        void *workspace, size_t workspace_bytes, int B, int H, int N, int d_k,
+                        float scale, bool need_qkv, bool need_o, bool need_dq)
+{
+    attn_status st = check_sizes(B, H, N, d_k, scale);
+    if (st != ATTN_OK) return st;
+    const void *ins_needed[6] = {need_qkv ? q : nullptr, need_qkv ? k : nullptr,
+                                 need_qkv ? v : nullptr, need_o ? o : nullptr, dout,
+                                 need_qkv ? static_cast<const void *>(lse) : nullptr};
+    if ((need_qkv && (!q || !k || !v || !lse || !dk || !dv)) || (need_o && !o) ||
+        ((need_qkv || need_o) && !dout) || (need_dq && !dq))
+        return ATTN_ERR_INVALID_ARG;
+    for (const void *p : {q, k, v, o, dout, static_cast<const void *>(lse),
+                          static_cast<const void *>(dq), static_cast<const void *>(dk),
+                          static_cast<const void *>(dv)})
+        if (p && !aligned16(p)) return ATTN_ERR_MISALIGNED;
+    const size_t need = attn_bwd_workspace_size(B, H, N, d_k);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
+        return ATTN_ERR_WORKSPACE;
+    const long long bh = (long long)B * H;
+    const size_t tbytes = (size_t)bh * N * d_k * 2, lbytes = (size_t)bh * N * 4;
+    Range outs[4];
+    int n_out = 0;
+    outs[n_out++] = span(workspace, need);
+    if (need_qkv) {
+        outs[n_out++] = span(dk, tbytes);
+        outs[n_out++] = span(dv, tbytes);
+    }
+    if (need_dq) outs[n_out++] = span(dq, tbytes);
+    for (int i = 0; i < n_out; ++i) {
+        for (int j = 0; j < 6; ++j) {
+            if (!ins_needed[j]) continue;
+            if (overlap(span(ins_needed[j], j == 5 ? lbytes : tbytes), outs[i])) return ATTN_ERR_INVALID_ARG;
+        }
+        for (int j = i + 1; j < n_out; ++j)
+            if (overlap(outs[i], outs[j])) return ATTN_ERR_INVALID_ARG;
+    }
+
+    DeviceState *dev = nullptr;
+    if ((st = device_state(&dev)) != ATTN_OK) return st;
+    std::memset(&a, 0, sizeof a);
+    if (need_qkv && (!make_map(&a.tm_q, q, (int)bh, N, d_k, 64) || !make_map(&a.tm_k, k, (int)bh, N, d_k, 128) ||
+                     !make_map(&a.tm_v, v, (int)bh, N, d_k, 128) ||
+                     !make_map(&a.tm_do, dout, (int)bh, N, d_k, 64)))
+        return fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
+    a.o = o;
+    a.dout = dout;
+    a.lse = lse;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.dvec = static_cast<float *>(workspace);
+    a.dq_acc = reinterpret_cast<float *>(static_cast<char *>(workspace) + align256((size_t)bh * N * 4));
+    a.bh = (int)bh;
+    a.n = N;
+    a.d = d_k;
+    a.scale = scale;
+    a.status = dev->status;
+    return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" attn_status attn_bwd_preprocess(const void *o, const void *dout, void *workspace,
+                                           size_t workspace_bytes, int B, int H, int N, int d_k,
+                                           cudaStream_t stream)
+{
+    BwdArgs a;
+    attn_status st = prepare_bwd(a, nullptr, nullptr, nullptr, o, dout, nullptr, nullptr, nullptr,
+                                 nullptr, workspace, workspace_bytes, B, H, N, d_k, 1.0f, false,
+                                 true, false);
+    if (st != ATTN_OK) return st;
+    const cudaError_t e = launch_bwd_preprocess(a, stream);
+    return e == cudaSuccess ? ATTN_OK : fail("attn_bwd_preprocess launch", e);
+}
+
+extern "C" attn_status attn_bwd_main(const void *q, const void *k, const void *v, const void *dout,
+                                     const float *lse, void *dk, void *dv, void *workspace,
+                                     size_t workspace_bytes, int B, int H, int N, int d_k,
+                                     float scale, cudaStream_t stream)
+{
+    BwdArgs a;
+    attn_status st = prepare_bwd(a, q, k, v, nullptr, dout, lse, nullptr, dk, dv, workspace,
+                                 workspace_bytes, B, H, N, d_k, scale, true, false, false);
+    if (st != ATTN_OK) return st;
+    const cudaError_t e = launch_bwd_main(a, stream);
+    return e == cudaSuccess ? ATTN_OK : fail("attn_bwd_main launch", e);
+}
+
+extern "C" attn_status attn_bwd_dq_convert(void *workspace, size_t workspace_bytes, void *dq,
+                                           int B, int H, int N, int d_k, float scale,
+                                           cudaStream_t stream)
+{
+    BwdArgs a;
+    attn_status st = prepare_bwd(a, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, dq,
+                                 nullptr, nullptr, workspace, workspace_bytes, B, H, N, d_k, scale,
+                                 false, false, true);
+    if (st != ATTN_OK) return st;
+    const cudaError_t e = launch_bwd_convert(a, stream);
+    return e == cudaSuccess ? ATTN_OK : fail("attn_bwd_dq_convert launch", e);
+}
+
+extern "C" attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
+                                const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                                void *workspace, size_t workspace_bytes, int B, int H, int N,
+                                int d_k, float scale, cudaStream_t stream)
+{
+    BwdArgs a;
+    attn_status st = prepare_bwd(a, q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes,
+                                 B, H, N, d_k, scale, true, true, true);
+    if (st != ATTN_OK) return st;
+    cudaError_t e = launch_bwd_preprocess(a, stream);
+    if (e == cudaSuccess) e = launch_bwd_main(a, stream);
+    if (e == cudaSuccess) e = launch_bwd_convert(a, stream);
+    return e == cudaSuccess ? ATTN_OK : fail("attn_bwd launch", e);
+}
+
+extern "C" attn_status attn_get_device_status(cudaStream_t stream)
+{
+    DeviceState *dev = nullptr;
+    attn_status st = device_state(&dev);
+    if (st != ATTN_OK) return st;
+    int word = 0;
+    cudaError_t e = cudaMemcpyAsync(&word, dev->status, sizeof(int), cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return fail("cudaMemcpyAsync(status)", e);
+    if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return fail("cudaStreamSynchronize", e);
+    if (word != 0) {
+        if ((e = cudaMemsetAsync(dev->status, 0, sizeof(int), stream)) != cudaSuccess ||
+            (e = cudaStreamSynchronize(stream)) != cudaSuccess)
+            return fail("clearing the status word", e);
+    }
+    return word == 0 ? ATTN_OK : static_cast<attn_status>(word);
+}
+
+extern "C" const char *attn_status_string(attn_status status)
+{
+    switch (status) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG: invalid argument";
+    case ATTN_ERR_UNSUPPORTED_DK: return "ATTN_ERR_UNSUPPORTED_DK: d_k must be 64 or 128";
+    case ATTN_ERR_MISALIGNED: return "ATTN_ERR_MISALIGNED: pointers must be 16-byte aligned";
+    case ATTN_ERR_LAUNCH: return "ATTN_ERR_LAUNCH: CUDA runtime error";
+    case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT: a kernel wait gave up";
+    case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case ATTN_ERR_DEVICE: return "ATTN_ERR_DEVICE: the current device is not an sm_103 GPU";
+    }
+    return "unknown attn_status";
+}
+
+extern "C" attn_status attn_debug_wait_timeout(unsigned limit_us, cudaStream_t stream)
+{
+    if (limit_us < 1 || limit_us > 1000000) return ATTN_ERR_INVALID_ARG;
+    DeviceState *dev = nullptr;
+    attn_status st = device_state(&dev);
+    if (st != ATTN_OK) return st;
+    const cudaError_t e = launch_wait_selftest(dev->status, (uint64_t)limit_us * 1000ull, stream);
+    return e == cudaSuccess ? ATTN_OK : fail("attn_debug_wait_timeout launch", e);
+}
+
+extern "C" const char *attn_last_error_string(void) { return t_last_error; }
+
+// --------------------------------------------------------------------------------------------
+// The wait self-test kernel: one thread waits on an mbarrier that nothing arrives on.
+namespace attn {
+namespace {
+__global__ void wait_selftest_kernel(int *status, uint64_t limit_ns)
+{
+    __shared__ uint64_t bar;
+    __shared__ int abort_sh;
+    abort_sh = 0;
+    ptx::mbar_init(&bar, 1);
+    ptx::fence_mbar_init();
+    const Guard g{&abort_sh, status, limit_ns};
+    wait_bounded(&bar, 0, g);
+}
+}  // namespace
+
+cudaError_t launch_wait_selftest(int *status, uint64_t limit_ns, cudaStream_t stream)
+{
+    wait_selftest_kernel<<<1, 1, 0, stream>>>(status, limit_ns);
+    return cudaGetLastError();
+}
+}  // namespace attn

@@ -1,0 +1,456 @@
+// Backward pass of exact multi-head attention for sm_103a.
+//
+// "Self-attention, CUDA kernels and FlashAttention", section 3 ("Recomputation in
+// backpropagation"): the forward pass keeps only a small per-row statistic (here LSE, the
+// natural-log log-sum-exp of each row of scaled scores); the backward pass recomputes the
+// attention tiles on chip from it instead of reading an N x N matrix from HBM.  The article
+// prints no gradient formulas; these are the chain rule on section 1's formulas:
+//   P = exp(scale * Q K^T - LSE),  dV = P^T dO,  dP = dO V^T,  D_i = sum_c dO_ic O_ic,
+//   dS = P o (dP - D),  dQ = scale * dS K,  dK = scale * dS^T Q.
+//
+// Three stream-ordered kernels:
+//   1. preprocess: D = rowsum(dO o O) (fp32) and zero the fp32 dQ accumulator.
+//   2. main: one CTA per 128-key tile j of one head, looping over all 64-row query tiles i.
+//        warp 8     TMA producer: K_j and V_j once; a ring of (Q_i, dO_i) tiles.
+//        warp 9     tcgen05 issuer, per query tile:
+//                     S^T = K_j Q_i^T, dP^T = V_j dO_i^T          (into TMEM, double-buffered)
+//                     dV += P^T dO_i  (P^T from TMEM), dK += dS^T Q_i, dQ_i^T = K_j^T dS^T
+//        warps 0-3  thread = key row: P^T = 2^(S^T c - LSE log2 e), dS^T = P^T o (dP^T - D);
+//                   P^T (bf16) goes back into TMEM over S^T, dS^T (bf16) into shared memory.
+//                   At the end they write dK (times scale) and dV in bf16.
+//        warps 4-7  thread = one of the d columns: move dQ_i^T from TMEM to shared memory
+//                   (transposed to dQ_i rows) and add it into the fp32 accumulator with one
+//                   bulk reduce-add per tile (fp32 atomics in L2: low bits vary run to run).
+//   3. convert: dQ = bf16(scale * accumulator).
+// TMEM columns: dK [0,d), dV [d,2d), then two buffers of {S^T/P^T (64), dP^T/dQ^T (64)}.
+// dQ^T has M = d rows; for d = 64 the MMA still runs with M = 128 and lanes 64-127 are unused.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace attn {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct BwdCfg {
+    static constexpr int BN = 128;   // keys per CTA (TMEM lanes of S^T, dP^T, dK, dV)
+    static constexpr int BM = 64;    // queries per inner tile
+    static constexpr int QST = (D == 64) ? 4 : 2;  // (Q, dO) ring depth
+    static constexpr int KV_BYTES = BN * D * 2;
+    static constexpr int Q_BYTES = BM * D * 2;
+    static constexpr int DS_BYTES = BN * BM * 2;
+    static constexpr int DQ_BYTES = BM * D * 4;
+    static constexpr int SMEM_BYTES = 2 * KV_BYTES + QST * 2 * Q_BYTES + 2 * DS_BYTES + DQ_BYTES + 1024;
+    static constexpr int THREADS = 320;
+    static constexpr uint32_t TM_DK = 0, TM_DV = D, TM_BUF = 2 * D;
+    __host__ __device__ static constexpr uint32_t tm_s(int b) { return TM_BUF + b * 128; }
+    __host__ __device__ static constexpr uint32_t tm_dp(int b) { return TM_BUF + b * 128 + 64; }
+};
+
+// ------------------------------------------------------------------ 1. preprocess
+template <int D>
+__global__ void __launch_bounds__(256)
+    bwd_preprocess_kernel(const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restrict__ dout,
+                          float *__restrict__ dvec, float *__restrict__ dq_acc, long long rows)
+{
+    // D: one group of D/8 threads per row, 8 bf16 (16 bytes) per thread.
+    constexpr int TPR = D / 8;
+    const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long nthreads = (long long)gridDim.x * blockDim.x;
+    // The loop runs whole warps in step (nthreads is a multiple of 32), so the shuffles below
+    // always see every lane of the warp.
+    const long long total = rows * TPR;
+    const long long bound = (total + 31) & ~31LL;
+    for (long long t = tid; t < bound; t += nthreads) {
+        const bool ok = t < total;
+        const long long row = t / TPR;
+        const int part = (int)(t % TPR);
+        float acc = 0.f;
+        if (ok) {
+            const uint4 a = *reinterpret_cast<const uint4 *>(o + row * D + part * 8);
+            const uint4 b = *reinterpret_cast<const uint4 *>(dout + row * D + part * 8);
+            const __nv_bfloat162 *a2 = reinterpret_cast<const __nv_bfloat162 *>(&a);
+            const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&b);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 fa = __bfloat1622float2(a2[e]);
+                const float2 fb = __bfloat1622float2(b2[e]);
+                acc = fmaf(fa.x, fb.x, acc);
+                acc = fmaf(fa.y, fb.y, acc);
+            }
+        }
+#pragma unroll
+        for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (ok && part == 0) dvec[row] = acc;
+    }
+    // zero the dQ accumulator (16 bytes per store)
+    float4 *acc4 = reinterpret_cast<float4 *>(dq_acc);
+    const long long n4 = rows * D / 4;
+    for (long long t = tid; t < n4; t += nthreads) acc4[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// ------------------------------------------------------------------ 3. dQ convert
+__global__ void __launch_bounds__(256)
+    bwd_convert_dq_kernel(const float *__restrict__ dq_acc, __nv_bfloat16 *__restrict__ dq,
+                          float scale, long long n8)
+{
+    const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long nthreads = (long long)gridDim.x * blockDim.x;
+    for (long long t = tid; t < n8; t += nthreads) {
+        const float4 a = reinterpret_cast<const float4 *>(dq_acc)[2 * t];
+        const float4 b = reinterpret_cast<const float4 *>(dq_acc)[2 * t + 1];
+        uint4 out;
+        out.x = ptx::pack_bf16x2(a.x * scale, a.y * scale);
+        out.y = ptx::pack_bf16x2(a.z * scale, a.w * scale);
+        out.z = ptx::pack_bf16x2(b.x * scale, b.y * scale);
+        out.w = ptx::pack_bf16x2(b.z * scale, b.w * scale);
+        reinterpret_cast<uint4 *>(dq)[t] = out;
+    }
+}
+
+// ------------------------------------------------------------------ 2. main
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+    bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const float *__restrict__ lse, const float *__restrict__ dvec,
+                    float *__restrict__ dq_acc, __nv_bfloat16 *__restrict__ dk,
+                    __nv_bfloat16 *__restrict__ dv, int n, int n_kvblocks, float scale,
+                    int *status)
+{
+    using C = BwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    uint8_t *sK = smem;
+    uint8_t *sV = sK + C::KV_BYTES;
+    uint8_t *sQ = sV + C::KV_BYTES;                 // QST stages of {Q_i, dO_i}
+    uint8_t *sDS = sQ + C::QST * 2 * C::Q_BYTES;    // two dS^T tiles
+    float *sDQ = reinterpret_cast<float *>(sDS + 2 * C::DS_BYTES);  // dQ_i staging [BM][D]
+
+    __shared__ uint64_t bar_kv, bar_qf[C::QST], bar_qe[C::QST];
+    __shared__ uint64_t bar_sdp[2], bar_ds_full[2], bar_ds_empty[2], bar_dq_full[2], bar_dq_empty[2];
+    __shared__ uint64_t bar_dkv, bar_done;
+    __shared__ float sLSE[2][C::BM], sDv[2][C::BM];
+    __shared__ uint32_t tmem_sh;
+    __shared__ int abort_sh;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.x / n_kvblocks;
+    const int kv0 = (blockIdx.x % n_kvblocks) * C::BN;
+    const int nq = (n + C::BM - 1) / C::BM;
+    const Guard g{&abort_sh, status, kWaitLimitNs};
+
+    if (threadIdx.x == 0) {
+        abort_sh = 0;
+        ptx::mbar_init(&bar_kv, 1);
+        for (int s = 0; s < C::QST; ++s) {
+            ptx::mbar_init(&bar_qf[s], 1);
+            ptx::mbar_init(&bar_qe[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(&bar_sdp[b], 1);
+            ptx::mbar_init(&bar_ds_full[b], 128);
+            ptx::mbar_init(&bar_ds_empty[b], 1);
+            ptx::mbar_init(&bar_dq_full[b], 1);
+            ptx::mbar_init(&bar_dq_empty[b], 128);
+        }
+        ptx::mbar_init(&bar_dkv, 1);
+        ptx::mbar_init(&bar_done, 1);
+        ptx::fence_mbar_init();
+    }
+    if (warp == 9) {
+        ptx::tmem_alloc(&tmem_sh, 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = tmem_sh;
+
+    if (warp == 8) {
+        // ---------------------------------------------------------------- TMA producer
+        if (ptx::elect_one()) {
+            ptx::tma_prefetch_desc(&tm_q);
+            ptx::tma_prefetch_desc(&tm_k);
+            ptx::tma_prefetch_desc(&tm_v);
+            ptx::tma_prefetch_desc(&tm_do);
+            ptx::mbar_arrive_expect_tx(&bar_kv, 2 * C::KV_BYTES);
+            for (int h = 0; h < D / 64; ++h) {
+                ptx::tma_load_3d(sK + h * C::BN * 128, &tm_k, &bar_kv, h * 64, kv0, bh);
+                ptx::tma_load_3d(sV + h * C::BN * 128, &tm_v, &bar_kv, h * 64, kv0, bh);
+            }
+            for (int it = 0; it < nq; ++it) {
+                const int s = it % C::QST;
+                const uint32_t ph = (it / C::QST) & 1;
+                wait_bounded(&bar_qe[s], ph ^ 1, g);
+                ptx::mbar_arrive_expect_tx(&bar_qf[s], 2 * C::Q_BYTES);
+                uint8_t *dq_tile = sQ + s * 2 * C::Q_BYTES;
+                for (int h = 0; h < D / 64; ++h) {
+                    ptx::tma_load_3d(dq_tile + h * C::BM * 128, &tm_q, &bar_qf[s], h * 64, it * C::BM, bh);
+                    ptx::tma_load_3d(dq_tile + C::Q_BYTES + h * C::BM * 128, &tm_do, &bar_qf[s],
+                                     h * 64, it * C::BM, bh);
+                }
+            }
+            wait_bounded(&bar_kv, 0, g);
+            for (int it = (nq > C::QST ? nq - C::QST : 0); it < nq; ++it)
+                wait_bounded(&bar_qf[it % C::QST], (it / C::QST) & 1, g);
+        }
+    } else if (warp == 9) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (ptx::elect_one()) {
+            const uint32_t idSdP = ptx::idesc_bf16_f32(128, C::BM, false, false);
+            const uint32_t idKV = ptx::idesc_bf16_f32(128, D, false, true);
+            const uint32_t idDQ = ptx::idesc_bf16_f32(128, C::BM, true, true);
+            const uint32_t k_base = ptx::smem_u32(sK), v_base = ptx::smem_u32(sV);
+            const uint32_t q_base = ptx::smem_u32(sQ), ds_base = ptx::smem_u32(sDS);
+            auto qs = [&](int s) { return q_base + s * 2 * C::Q_BYTES; };
+            auto dos = [&](int s) { return q_base + s * 2 * C::Q_BYTES + C::Q_BYTES; };
+            // S^T = K_j Q_i^T and dP^T = V_j dO_i^T: all four operands K-major over d.
+            auto issue_sdp = [&](int s, int b) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t offa = (kk >> 2) * (C::BN * 128) + (kk & 3) * 32;
+                    const uint32_t offb = (kk >> 2) * (C::BM * 128) + (kk & 3) * 32;
+                    ptx::mma_ss(tmem + C::tm_s(b), ptx::sdesc_sw128(k_base + offa, 16, 1024),
+                                ptx::sdesc_sw128(qs(s) + offb, 16, 1024), idSdP, kk > 0 ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t offa = (kk >> 2) * (C::BN * 128) + (kk & 3) * 32;
+                    const uint32_t offb = (kk >> 2) * (C::BM * 128) + (kk & 3) * 32;
+                    ptx::mma_ss(tmem + C::tm_dp(b), ptx::sdesc_sw128(v_base + offa, 16, 1024),
+                                ptx::sdesc_sw128(dos(s) + offb, 16, 1024), idSdP, kk > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_grads = [&](int s, int b, bool acc) {
+                // dV += P^T dO_i: A = P^T (TMEM, 8 columns per 16 queries), B = dO_i MN-major.
+#pragma unroll
+                for (int kk = 0; kk < C::BM / 16; ++kk)
+                    ptx::mma_ts(tmem + C::TM_DV, tmem + C::tm_s(b) + kk * 8,
+                                ptx::sdesc_sw128(dos(s) + kk * 2048, C::BM * 128, 1024), idKV,
+                                (acc || kk > 0) ? 1u : 0u);
+                // dK += dS^T Q_i: A = dS^T K-major (queries contiguous), B = Q_i MN-major.
+#pragma unroll
+                for (int kk = 0; kk < C::BM / 16; ++kk)
+                    ptx::mma_ss(tmem + C::TM_DK, ptx::sdesc_sw128(ds_base + b * C::DS_BYTES + kk * 32, 16, 1024),
+                                ptx::sdesc_sw128(qs(s) + kk * 2048, C::BM * 128, 1024), idKV,
+                                (acc || kk > 0) ? 1u : 0u);
+                // dQ_i^T = K_j^T dS^T: A = K_j MN-major (M = d; halves BN*128 bytes apart),
+                // B = dS^T MN-major (N = 64 queries), K = 128 keys.
+#pragma unroll
+                for (int kk = 0; kk < C::BN / 16; ++kk)
+                    ptx::mma_ss(tmem + C::tm_dp(b), ptx::sdesc_sw128(k_base + kk * 2048, C::BN * 128, 1024),
+                                ptx::sdesc_sw128(ds_base + b * C::DS_BYTES + kk * 2048, C::BN * 128, 1024),
+                                idDQ, kk > 0 ? 1u : 0u);
+            };
+            wait_bounded(&bar_kv, 0, g);
+            wait_bounded(&bar_qf[0], 0, g);
+            ptx::tc_fence_after();
+            issue_sdp(0, 0);
+            ptx::mma_commit(&bar_sdp[0]);
+            for (int it = 0; it < nq; ++it) {
+                const int b = it & 1, s = it % C::QST;
+                if (it + 1 < nq) {
+                    const int s1 = (it + 1) % C::QST, b1 = b ^ 1;
+                    wait_bounded(&bar_qf[s1], ((it + 1) / C::QST) & 1, g);
+                    wait_bounded(&bar_dq_empty[b1], (((it + 1) >> 1) & 1) ^ 1, g);
+                    ptx::tc_fence_after();
+                    issue_sdp(s1, b1);
+                    ptx::mma_commit(&bar_sdp[b1]);
+                }
+                wait_bounded(&bar_ds_full[b], (it >> 1) & 1, g);
+                ptx::tc_fence_after();
+                issue_grads(s, b, it > 0);
+                ptx::mma_commit(&bar_dq_full[b]);
+                ptx::mma_commit(&bar_qe[s]);
+                ptx::mma_commit(&bar_ds_empty[b]);
+            }
+            ptx::mma_commit(&bar_dkv);
+            ptx::mma_commit(&bar_done);
+            wait_bounded(&bar_done, 0, g);
+        }
+    } else if (warp < 4) {
+        // ---------------------------------------------------------------- P / dS warpgroup
+        const int r = warp * 32 + lane;     // key row within the tile = TMEM lane
+        const bool key_ok = kv0 + r < n;
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const float scale_log2 = scale * kLog2e;
+        for (int it = 0; it < nq; ++it) {
+            const int b = it & 1;
+            const uint32_t ph = (it >> 1) & 1;
+            {   // this tile's LSE (log2 units) and D into shared memory
+                const int c = threadIdx.x & 63;
+                const int qi = it * C::BM + c;
+                if (threadIdx.x < 64)
+                    sLSE[b][c] = qi < n ? lse[(size_t)bh * n + qi] * kLog2e : INFINITY;
+                else
+                    sDv[b][c] = qi < n ? dvec[(size_t)bh * n + qi] : 0.f;
+            }
+            ptx::named_bar(1, 128);
+            wait_bounded(&bar_sdp[b], ph, g);
+            ptx::tc_fence_after();
+            uint32_t pp[32], dsp[32];
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t sv[32], dpv[32];
+                ptx::tmem_ld32(tmem + lane_off + C::tm_s(b) + half * 32, sv);
+                ptx::tmem_ld32(tmem + lane_off + C::tm_dp(b) + half * 32, dpv);
+                ptx::tmem_ld_wait();
+                reg_fence(sv);
+                reg_fence(dpv);
+#pragma unroll
+                for (int c = 0; c < 32; c += 2) {
+                    const int q = half * 32 + c;
+                    float p0 = ptx::ex2(fmaf(__uint_as_float(sv[c]), scale_log2, -sLSE[b][q]));
+                    float p1 = ptx::ex2(fmaf(__uint_as_float(sv[c + 1]), scale_log2, -sLSE[b][q + 1]));
+                    if (!key_ok) p0 = p1 = 0.f;
+                    const float ds0 = p0 * (__uint_as_float(dpv[c]) - sDv[b][q]);
+                    const float ds1 = p1 * (__uint_as_float(dpv[c + 1]) - sDv[b][q + 1]);
+                    pp[q >> 1] = ptx::pack_bf16x2(p0, p1);
+                    dsp[q >> 1] = ptx::pack_bf16x2(ds0, ds1);
+                }
+            }
+            ptx::tmem_st32(tmem + lane_off + C::tm_s(b), pp);
+            wait_bounded(&bar_ds_empty[b], ph ^ 1, g);
+            uint8_t *rowp = sDS + b * C::DS_BYTES + r * 128;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch)
+                *reinterpret_cast<uint4 *>(rowp + ((ch ^ (r & 7)) << 4)) =
+                    make_uint4(dsp[4 * ch], dsp[4 * ch + 1], dsp[4 * ch + 2], dsp[4 * ch + 3]);
+            ptx::tmem_st_wait();
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&bar_ds_full[b]);
+        }
+        // epilogue: dK = scale * acc, dV = acc, bf16, key rows < n
+        wait_bounded(&bar_dkv, 0, g);
+        ptx::tc_fence_after();
+        const size_t row_off = ((size_t)bh * n + (key_ok ? kv0 + r : 0)) * D;
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+            const float mul = which == 0 ? scale : 1.f;
+            __nv_bfloat16 *dst_row = (which == 0 ? dk : dv) + row_off;
+            const uint32_t col0 = which == 0 ? C::TM_DK : C::TM_DV;
+#pragma unroll
+            for (int c = 0; c < D; c += 32) {
+                uint32_t v[32];
+                ptx::tmem_ld32(tmem + lane_off + col0 + c, v);
+                ptx::tmem_ld_wait();
+                reg_fence(v);
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    pk[e] = ptx::pack_bf16x2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+                if (key_ok) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(dst_row + c);
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4)
+                        dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                }
+            }
+        }
+    } else {
+        // ---------------------------------------------------------------- dQ warpgroup
+        const int r = (warp - 4) * 32 + lane;   // d column = TMEM lane of dQ^T
+        const uint32_t lane_off = (uint32_t)((warp - 4) * 32) << 16;
+        const bool leader = threadIdx.x == 128;
+        for (int it = 0; it < nq; ++it) {
+            const int b = it & 1;
+            wait_bounded(&bar_dq_full[b], (it >> 1) & 1, g);
+            ptx::tc_fence_after();
+            uint32_t v[64];
+            if ((warp - 4) * 32 < D) {
+                uint32_t (&v0)[32] = *reinterpret_cast<uint32_t (*)[32]>(&v[0]);
+                uint32_t (&v1)[32] = *reinterpret_cast<uint32_t (*)[32]>(&v[32]);
+                ptx::tmem_ld32(tmem + lane_off + C::tm_dp(b), v0);
+                ptx::tmem_ld32(tmem + lane_off + C::tm_dp(b) + 32, v1);
+                ptx::tmem_ld_wait();
+                reg_fence(v);
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&bar_dq_empty[b]);
+            if (leader) ptx::bulk_wait_group_read<0>();   // staging buffer free again
+            ptx::named_bar(2, 128);
+            if (r < D) {
+#pragma unroll
+                for (int c = 0; c < C::BM; ++c) sDQ[c * D + r] = __uint_as_float(v[c]);
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::named_bar(2, 128);
+            if (leader) {
+                const int q0 = it * C::BM;
+                const int rows = (n - q0) < C::BM ? (n - q0) : C::BM;
+                ptx::bulk_reduce_add_f32(dq_acc + ((size_t)bh * n + q0) * D, sDQ, (uint32_t)rows * D * 4);
+                ptx::bulk_commit_group();
+            }
+        }
+        if (leader) ptx::bulk_wait_group<0>();
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 9) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 512);
+    }
+}
+
+int g_num_sms = 0;
+
+int elementwise_blocks()
+{
+    if (g_num_sms == 0) {
+        int dev = 0, sms = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        g_num_sms = sms > 0 ? sms : 148;
+    }
+    return 4 * g_num_sms;
+}
+
+template <int D>
+cudaError_t launch_preprocess_d(const BwdArgs &a, cudaStream_t stream)
+{
+    bwd_preprocess_kernel<D><<<elementwise_blocks(), 256, 0, stream>>>(
+        reinterpret_cast<const __nv_bfloat16 *>(a.o), reinterpret_cast<const __nv_bfloat16 *>(a.dout),
+        a.dvec, a.dq_acc, (long long)a.bh * a.n);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_main_d(const BwdArgs &a, cudaStream_t stream)
+{
+    using C = BwdCfg<D>;
+    cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int n_kvblocks = (a.n + C::BN - 1) / C::BN;
+    const long long ctas = (long long)n_kvblocks * a.bh;
+    bwd_main_kernel<D><<<(unsigned)ctas, C::THREADS, C::SMEM_BYTES, stream>>>(
+        a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse, a.dvec, a.dq_acc,
+        reinterpret_cast<__nv_bfloat16 *>(a.dk), reinterpret_cast<__nv_bfloat16 *>(a.dv), a.n,
+        n_kvblocks, a.scale, a.status);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_preprocess(const BwdArgs &a, cudaStream_t stream)
+{
+    return a.d == 64 ? launch_preprocess_d<64>(a, stream) : launch_preprocess_d<128>(a, stream);
+}
+
+cudaError_t launch_bwd_main(const BwdArgs &a, cudaStream_t stream)
+{
+    return a.d == 64 ? launch_main_d<64>(a, stream) : launch_main_d<128>(a, stream);
+}
+
+cudaError_t launch_bwd_convert(const BwdArgs &a, cudaStream_t stream)
+{
+    bwd_convert_dq_kernel<<<elementwise_blocks(), 256, 0, stream>>>(
+        a.dq_acc, reinterpret_cast<__nv_bfloat16 *>(a.dq), a.scale, (long long)a.bh * a.n * a.d / 8);
+    return cudaGetLastError();
+}
+
+}  // namespace attn

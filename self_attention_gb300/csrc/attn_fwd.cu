@@ -1,0 +1,343 @@
+// Forward pass of exact multi-head attention, O = softmax(scale * Q K^T) V, plus the per-row
+// log-sum-exp of the scaled scores, for sm_103a.
+//
+// "Self-attention, CUDA kernels and FlashAttention", section 1 defines the result (the
+// "Scores" formula with the division by sqrt(d_k), the row softmax, Attention(Q,K,V) and
+// independent heads).  Section 3 describes how to reach it without ever writing the N x N
+// score matrix to HBM: Q, K and V are cut into blocks that fit on chip ("Tiling"), and the
+// softmax runs online, keeping a running maximum and normaliser per row and rescaling the
+// partial output when a new block raises the maximum ("The online softmax trick").  The
+// per-row statistic the backward pass needs ("Recomputation in backpropagation") is stored
+// as LSE = log sum_j exp(scale * q_i . k_j).
+//
+// Blackwell mapping (one CTA = 256 query rows of one head, two tiles of 128):
+//   warp 8      TMA producer: Q tiles once, then a ring of K and V tiles (128 keys each).
+//   warp 9      tcgen05 issuer: S_t = Q_t K_j^T into TMEM (fp32), then O_t += P_t V_j with
+//               P_t read from TMEM (bf16, written over S_t) and V_j from shared memory.
+//   warps 0-7   two softmax warpgroups, one per query tile; thread = one query row.  They
+//               read S_t from TMEM, update the running max m (log2 units, scale folded into
+//               log2 e) and sum l, write P_t = 2^(x - m) as bf16 back into TMEM and rescale
+//               O_t in TMEM when the maximum grew by more than kTau (exact: the final
+//               division uses the same m).  The two tiles alternate on the tensor core, so
+//               one tile's softmax overlaps the other tile's matrix products.
+// TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+d), O_1 [256+d,256+2d).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace attn {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+// The running maximum is only moved (and O rescaled) when a tile raises it by more than this
+// many powers of two; in between, probabilities may reach 2^kTau, far from fp32/bf16 limits.
+constexpr float kTau = 8.0f;
+
+template <int D>
+struct FwdCfg {
+    static constexpr int BM = 128;  // query rows per tile (= TMEM lanes)
+    static constexpr int NQ = 2;    // query tiles per CTA
+    static constexpr int BN = 128;  // keys per K/V tile
+    static constexpr int STAGES = (D == 64) ? 4 : 2;
+    static constexpr int Q_BYTES = BM * D * 2;
+    static constexpr int KV_BYTES = BN * D * 2;
+    static constexpr int SMEM_BYTES = NQ * Q_BYTES + 2 * STAGES * KV_BYTES + 1024;
+    static constexpr int THREADS = 320;
+    static constexpr uint32_t TM_O = 256;  // first O column
+};
+
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16 *__restrict__ o,
+               float *__restrict__ lse, int n, int n_qblocks, float scale_log2, int *status)
+{
+    using C = FwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    uint8_t *sQ = smem;
+    uint8_t *sK = sQ + C::NQ * C::Q_BYTES;
+    uint8_t *sV = sK + C::STAGES * C::KV_BYTES;
+
+    __shared__ uint64_t bar_q;
+    __shared__ uint64_t bar_kf[C::STAGES], bar_ke[C::STAGES], bar_vf[C::STAGES], bar_ve[C::STAGES];
+    __shared__ uint64_t bar_s[2], bar_p[2], bar_o[2], bar_done;
+    __shared__ uint32_t tmem_sh;
+    __shared__ int abort_sh;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.x / n_qblocks;
+    const int q0 = (blockIdx.x % n_qblocks) * (C::NQ * C::BM);
+    const int nkv = (n + C::BN - 1) / C::BN;
+    const Guard g{&abort_sh, status, kWaitLimitNs};
+
+    if (threadIdx.x == 0) {
+        abort_sh = 0;
+        ptx::mbar_init(&bar_q, 1);
+        for (int s = 0; s < C::STAGES; ++s) {
+            ptx::mbar_init(&bar_kf[s], 1);
+            ptx::mbar_init(&bar_ke[s], 1);
+            ptx::mbar_init(&bar_vf[s], 1);
+            ptx::mbar_init(&bar_ve[s], 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            ptx::mbar_init(&bar_s[t], 1);
+            ptx::mbar_init(&bar_p[t], 128);
+            ptx::mbar_init(&bar_o[t], 1);
+        }
+        ptx::mbar_init(&bar_done, 1);
+        ptx::fence_mbar_init();
+    }
+    if (warp == 9) {
+        ptx::tmem_alloc(&tmem_sh, 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = tmem_sh;
+
+    if (warp == 8) {
+        // ---------------------------------------------------------------- TMA producer
+        if (ptx::elect_one()) {
+            ptx::tma_prefetch_desc(&tm_q);
+            ptx::tma_prefetch_desc(&tm_k);
+            ptx::tma_prefetch_desc(&tm_v);
+            ptx::mbar_arrive_expect_tx(&bar_q, C::NQ * C::Q_BYTES);
+            for (int t = 0; t < C::NQ; ++t)
+                for (int h = 0; h < D / 64; ++h)
+                    ptx::tma_load_3d(sQ + t * C::Q_BYTES + h * C::BM * 128, &tm_q, &bar_q, h * 64,
+                                     q0 + t * C::BM, bh);
+            for (int j = 0; j < nkv; ++j) {
+                const int s = j % C::STAGES;
+                const uint32_t ph = (j / C::STAGES) & 1;
+                wait_bounded(&bar_ke[s], ph ^ 1, g);
+                ptx::mbar_arrive_expect_tx(&bar_kf[s], C::KV_BYTES);
+                for (int h = 0; h < D / 64; ++h)
+                    ptx::tma_load_3d(sK + s * C::KV_BYTES + h * C::BN * 128, &tm_k, &bar_kf[s],
+                                     h * 64, j * C::BN, bh);
+                wait_bounded(&bar_ve[s], ph ^ 1, g);
+                ptx::mbar_arrive_expect_tx(&bar_vf[s], C::KV_BYTES);
+                for (int h = 0; h < D / 64; ++h)
+                    ptx::tma_load_3d(sV + s * C::KV_BYTES + h * C::BN * 128, &tm_v, &bar_vf[s],
+                                     h * 64, j * C::BN, bh);
+            }
+            // Do not leave the CTA with copies in flight (matters only after a timeout).
+            for (int j = (nkv > C::STAGES ? nkv - C::STAGES : 0); j < nkv; ++j) {
+                const int s = j % C::STAGES;
+                const uint32_t ph = (j / C::STAGES) & 1;
+                wait_bounded(&bar_kf[s], ph, g);
+                wait_bounded(&bar_vf[s], ph, g);
+            }
+        }
+    } else if (warp == 9) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (ptx::elect_one()) {
+            const uint32_t idS = ptx::idesc_bf16_f32(128, C::BN, false, false);
+            const uint32_t idO = ptx::idesc_bf16_f32(128, D, false, true);
+            const uint32_t q_base = ptx::smem_u32(sQ), k_base = ptx::smem_u32(sK),
+                           v_base = ptx::smem_u32(sV);
+            // S_t = Q_t K^T: both operands K-major (d contiguous), 64-column halves for d=128.
+            auto issue_s = [&](int t, int s) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * (C::BM * 128) + (kk & 3) * 32;
+                    const uint64_t a = ptx::sdesc_sw128(q_base + t * C::Q_BYTES + off, 16, 1024);
+                    const uint64_t b = ptx::sdesc_sw128(k_base + s * C::KV_BYTES + off, 16, 1024);
+                    ptx::mma_ss(tmem + t * 128, a, b, idS, kk > 0 ? 1u : 0u);
+                }
+            };
+            // O_t += P_t V: P from TMEM (8 columns = 16 keys per step), V MN-major (d contiguous).
+            auto issue_pv = [&](int t, int s, bool acc) {
+#pragma unroll
+                for (int kk = 0; kk < C::BN / 16; ++kk) {
+                    const uint64_t b =
+                        ptx::sdesc_sw128(v_base + s * C::KV_BYTES + kk * 2048, C::BN * 128, 1024);
+                    ptx::mma_ts(tmem + C::TM_O + t * D, tmem + t * 128 + kk * 8, b, idO,
+                                (acc || kk > 0) ? 1u : 0u);
+                }
+            };
+            wait_bounded(&bar_q, 0, g);
+            wait_bounded(&bar_kf[0], 0, g);
+            ptx::tc_fence_after();
+            issue_s(0, 0);
+            ptx::mma_commit(&bar_s[0]);
+            issue_s(1, 0);
+            ptx::mma_commit(&bar_s[1]);
+            ptx::mma_commit(&bar_ke[0]);
+            for (int j = 0; j < nkv; ++j) {
+                const int s = j % C::STAGES;
+                const uint32_t ph = (j / C::STAGES) & 1;
+                const int jn = j + 1;
+                const int sn = jn % C::STAGES;
+                const uint32_t phn = (jn / C::STAGES) & 1;
+                wait_bounded(&bar_vf[s], ph, g);
+                wait_bounded(&bar_p[0], j & 1, g);
+                ptx::tc_fence_after();
+                issue_pv(0, s, j > 0);
+                if (jn < nkv) {
+                    wait_bounded(&bar_kf[sn], phn, g);
+                    ptx::tc_fence_after();
+                    issue_s(0, sn);
+                    ptx::mma_commit(&bar_s[0]);
+                } else {
+                    ptx::mma_commit(&bar_o[0]);
+                }
+                wait_bounded(&bar_p[1], j & 1, g);
+                ptx::tc_fence_after();
+                issue_pv(1, s, j > 0);
+                ptx::mma_commit(&bar_ve[s]);
+                if (jn < nkv) {
+                    issue_s(1, sn);
+                    ptx::mma_commit(&bar_s[1]);
+                    ptx::mma_commit(&bar_ke[sn]);
+                } else {
+                    ptx::mma_commit(&bar_o[1]);
+                }
+            }
+            // Every MMA must have finished before TMEM is released (matters after a timeout).
+            ptx::mma_commit(&bar_done);
+            wait_bounded(&bar_done, 0, g);
+        }
+    } else {
+        // ---------------------------------------------------------------- softmax warpgroups
+        const int t = warp >> 2;
+        const int quarter = warp & 3;
+        const int row = q0 + t * C::BM + quarter * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t tS = tmem + lane_off + t * 128;
+        const uint32_t tO = tmem + lane_off + C::TM_O + t * D;
+        float m = -INFINITY, l = 0.f;
+
+        for (int j = 0; j < nkv; ++j) {
+            wait_bounded(&bar_s[t], j & 1, g);
+            ptx::tc_fence_after();
+            uint32_t r[128];
+            {
+                uint32_t (&r0)[32] = *reinterpret_cast<uint32_t (*)[32]>(&r[0]);
+                uint32_t (&r1)[32] = *reinterpret_cast<uint32_t (*)[32]>(&r[32]);
+                uint32_t (&r2)[32] = *reinterpret_cast<uint32_t (*)[32]>(&r[64]);
+                uint32_t (&r3)[32] = *reinterpret_cast<uint32_t (*)[32]>(&r[96]);
+                ptx::tmem_ld32(tS + 0, r0);
+                ptx::tmem_ld32(tS + 32, r1);
+                ptx::tmem_ld32(tS + 64, r2);
+                ptx::tmem_ld32(tS + 96, r3);
+                ptx::tmem_ld_wait();
+                reg_fence(r);
+            }
+            // keys >= n (only in the last tile) take no weight
+            const int valid = n - j * C::BN;
+            if (valid < C::BN) {
+#pragma unroll
+                for (int i = 0; i < 128; ++i)
+                    if (i >= valid) r[i] = __float_as_uint(-INFINITY);
+            }
+            float mx[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) mx[u] = __uint_as_float(r[u]);
+#pragma unroll
+            for (int i = 8; i < 128; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(r[i]));
+            const float smax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                     fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+            const float mt = smax * scale_log2;
+            float m_new = m, alpha = 1.f;
+            bool rescale = false;
+            if (j == 0) {
+                m_new = mt;
+            } else if (__any_sync(0xffffffffu, mt > m + kTau)) {
+                m_new = fmaxf(m, mt);
+                alpha = ptx::ex2(m - m_new);
+                rescale = true;
+            }
+            const float neg_m = -m_new;
+            float sum[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t pk0[32], pk1[32];
+#pragma unroll
+            for (int i = 0; i < 128; i += 2) {
+                const float p0 = ptx::ex2(fmaf(__uint_as_float(r[i]), scale_log2, neg_m));
+                const float p1 = ptx::ex2(fmaf(__uint_as_float(r[i + 1]), scale_log2, neg_m));
+                sum[(i >> 1) & 3] += p0 + p1;
+                if (i < 64)
+                    pk0[i >> 1] = ptx::pack_bf16x2(p0, p1);
+                else
+                    pk1[(i - 64) >> 1] = ptx::pack_bf16x2(p0, p1);
+            }
+            l = l * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
+            m = m_new;
+            if (rescale) {
+#pragma unroll
+                for (int c = 0; c < D; c += 32) {
+                    uint32_t ov[32];
+                    ptx::tmem_ld32(tO + c, ov);
+                    ptx::tmem_ld_wait();
+                    reg_fence(ov);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                    ptx::tmem_st32(tO + c, ov);
+                }
+            }
+            ptx::tmem_st32(tS + 0, pk0);
+            ptx::tmem_st32(tS + 32, pk1);
+            ptx::tmem_st_wait();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&bar_p[t]);
+        }
+
+        // epilogue: O = O_acc / l (bf16), LSE = (m + log2 l) ln 2
+        wait_bounded(&bar_o[t], 0, g);
+        ptx::tc_fence_after();
+        const float inv_l = 1.f / l;
+        __nv_bfloat16 *orow = o + ((size_t)bh * n + (row < n ? row : 0)) * D;
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+            uint32_t ov[32];
+            ptx::tmem_ld32(tO + c, ov);
+            ptx::tmem_ld_wait();
+            reg_fence(ov);
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                pk[i] = ptx::pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l,
+                                         __uint_as_float(ov[2 * i + 1]) * inv_l);
+            if (row < n) {
+                uint4 *dst = reinterpret_cast<uint4 *>(orow + c);
+#pragma unroll
+                for (int v4 = 0; v4 < 4; ++v4)
+                    dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+            }
+        }
+        if (row < n) lse[(size_t)bh * n + row] = (m + log2f(l)) * kLn2;
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 9) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const FwdArgs &a, cudaStream_t stream)
+{
+    using C = FwdCfg<D>;
+    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int rows_per_cta = C::NQ * C::BM;
+    const int n_qblocks = (a.n + rows_per_cta - 1) / rows_per_cta;
+    const long long ctas = (long long)n_qblocks * a.bh;
+    fwd_kernel<D><<<(unsigned)ctas, C::THREADS, C::SMEM_BYTES, stream>>>(
+        a.tm_q, a.tm_k, a.tm_v, reinterpret_cast<__nv_bfloat16 *>(a.o), a.lse, a.n, n_qblocks,
+        a.scale * kLog2e, a.status);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdArgs &a, cudaStream_t stream)
+{
+    return a.d == 64 ? launch_fwd_d<64>(a, stream) : launch_fwd_d<128>(a, stream);
+}
+
+}  // namespace attn

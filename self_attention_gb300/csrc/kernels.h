@@ -1,0 +1,39 @@
+// Host-side launchers of the attention kernels (internal to the library; the public C ABI
+// in include/attn.h validates arguments and calls these).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace attn {
+
+struct FwdArgs {
+    CUtensorMap tm_q, tm_k, tm_v;   // 3-D maps over [BH, N, d] bf16, 64 x rows boxes, 128-byte swizzle
+    void *o;                        // [BH, N, d] bf16
+    float *lse;                     // [BH, N] fp32
+    int bh, n, d;
+    float scale;
+    int *status;                    // device status word
+};
+
+struct BwdArgs {
+    CUtensorMap tm_q, tm_k, tm_v, tm_do;
+    const void *o, *dout;           // [BH, N, d] bf16
+    const float *lse;               // [BH, N]
+    void *dq, *dk, *dv;             // [BH, N, d] bf16
+    float *dvec;                    // [BH, N]   workspace: rowsum(dO o O)
+    float *dq_acc;                  // [BH, N, d] workspace: fp32 dQ accumulator
+    int bh, n, d;
+    float scale;
+    int *status;
+};
+
+cudaError_t launch_fwd(const FwdArgs &a, cudaStream_t stream);
+// The three stream-ordered phases of the backward pass.
+cudaError_t launch_bwd_preprocess(const BwdArgs &a, cudaStream_t stream);
+cudaError_t launch_bwd_main(const BwdArgs &a, cudaStream_t stream);
+cudaError_t launch_bwd_convert(const BwdArgs &a, cudaStream_t stream);
+cudaError_t launch_wait_selftest(int *status, uint64_t limit_ns, cudaStream_t stream);
+
+}  // namespace attn

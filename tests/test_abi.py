@@ -1,0 +1,108 @@
+"""The C-ABI library without a GPU: it loads, exports every function include/attn.h declares,
+and rejects bad arguments with the documented status before touching the device."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import self_attention_gb300 as sa
+from self_attention_gb300.build import INCLUDE, build
+
+HEADER = os.path.join(INCLUDE, "attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return sa.load_library(build())
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_get_device_status",
+                     "attn_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", build()], capture_output=True,
+                         text=True).stdout
+    exported = set(re.findall(r"\bT (attn_\w+)$", out, flags=re.M))
+    for name in declared_functions():
+        assert name in exported, f"{name} declared in attn.h but not exported"
+        assert hasattr(lib, name)
+    assert set(sa.EXPORTS) <= exported
+
+
+def test_status_strings(lib):
+    for code, name in sa.STATUS.items():
+        assert sa.attn_status_string(code).startswith(name)
+
+
+def test_workspace_size(lib):
+    a256 = lambda x: (x + 255) // 256 * 256
+    assert sa.attn_bwd_workspace_size(1, 1, 100, 64) == a256(100 * 4) + a256(100 * 64 * 4)
+    assert sa.attn_bwd_workspace_size(2, 16, 16384, 128) == a256(2 * 16 * 16384 * 4) + a256(2 * 16 * 16384 * 128 * 4)
+    assert sa.attn_bwd_workspace_size(1, 1, 100, 96) == 0
+    assert sa.attn_bwd_workspace_size(0, 1, 100, 64) == 0
+
+
+# Fake, never-dereferenced device addresses: validation fails before any CUDA call.
+Q, K, V, O, L = (0x10000000 * (i + 1) for i in range(5))
+
+
+def _fwd(lib, q=Q, k=K, v=V, o=O, lse=L, B=1, H=2, N=64, d=64, scale=0.125):
+    return lib.attn_fwd(q, k, v, o, lse, B, H, N, d, ctypes.c_float(scale), None)
+
+
+def test_fwd_argument_errors(lib):
+    assert _fwd(lib, d=96) == 2
+    assert _fwd(lib, d=0) == 2
+    assert _fwd(lib, B=0) == 1
+    assert _fwd(lib, N=0) == 1
+    assert _fwd(lib, H=-1) == 1
+    assert _fwd(lib, scale=float("nan")) == 1
+    assert _fwd(lib, scale=0.0) == 1
+    assert _fwd(lib, scale=float("inf")) == 1
+    assert _fwd(lib, q=0) == 1
+    assert _fwd(lib, lse=0) == 1
+    assert _fwd(lib, q=Q + 8) == 3
+    assert _fwd(lib, lse=L + 4) == 3
+    assert _fwd(lib, o=Q) == 1                 # output aliases an input
+    assert _fwd(lib, lse=O + 64) == 1          # lse inside o
+    assert _fwd(lib, B=1 << 20, H=1 << 20) == 1
+
+
+def test_bwd_argument_errors(lib):
+    ws = 0x70000000
+    need = sa.attn_bwd_workspace_size(1, 2, 64, 64)
+    dq, dk, dv = 0x80000000, 0x90000000, 0xA0000000
+
+    def bwd(ws=ws, nbytes=need, d=64, dq=dq, o=O):
+        return lib.attn_bwd(Q, K, V, o, 0x60000000, L, dq, dk, dv, ws, nbytes, 1, 2, 64, d,
+                            ctypes.c_float(0.125), None)
+
+    assert bwd(d=80) == 2
+    assert bwd(nbytes=need - 1) == 6
+    assert bwd(ws=0) == 6
+    assert bwd(ws=ws + 16) == 6
+    assert bwd(dq=Q) == 1
+    assert bwd(dq=dk) == 1
+    assert bwd(dq=dq + 2) == 3
+    assert bwd(o=0) == 1
+    assert lib.attn_bwd_main(Q, K, V, 0x60000000, L, dk, dv, ws, need - 16, 1, 2, 64, 64,
+                             ctypes.c_float(0.125), None) == 6
+    assert lib.attn_bwd_preprocess(O, 0, ws, need, 1, 2, 64, 64, None) == 1
+    assert lib.attn_bwd_dq_convert(ws, need, 0, 1, 2, 64, 64, ctypes.c_float(0.125), None) == 1
+
+
+def test_debug_timeout_argument_range(lib):
+    assert lib.attn_debug_wait_timeout(0, None) == 1
+    assert lib.attn_debug_wait_timeout(10 ** 7, None) == 1

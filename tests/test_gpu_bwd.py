@@ -1,0 +1,174 @@
+"""Backward parity: dQ, dK, dV from the CUDA path (through the C ABI) against the fp64 oracle
+on the same seeded bf16 inputs.  The GPU backward consumes the GPU forward's bf16 O and
+fp32 LSE, exactly as a training step does; the oracle uses its own fp64 forward."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import self_attention_gb300 as sa
+from self_attention_gb300.inputs import WORKLOADS, make_qkv, make_workload_inputs
+from _compare import check_grad
+
+pytestmark = pytest.mark.gpu
+
+GUARD = 16384
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from self_attention_gb300.build import build
+    sa.load_library(build())
+
+
+def _guarded(shape, dtype):
+    n = int(np.prod(shape))
+    buf = torch.full((n + 2 * GUARD,), float("nan"), dtype=dtype, device="cuda")
+    return buf, buf[GUARD:GUARD + n].view(shape)
+
+
+def _intact(buf):
+    return bool(torch.isnan(torch.cat([buf[:GUARD], buf[-GUARD:]])).all())
+
+
+def run_fwd_bwd(inp, scale):
+    q, k, v, do = (inp[x].cuda() for x in ("q", "k", "v", "do"))
+    B, H, N, D = q.shape
+    o, lse = sa.forward(q, k, v, scale)
+    bufs = [_guarded((B, H, N, D), torch.bfloat16) for _ in range(3)]
+    dq, dk, dv = (b[1] for b in bufs)
+    ws_bytes = sa.attn_bwd_workspace_size(B, H, N, D)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    sa.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, ws_bytes, B, H, N, D, scale)
+    assert sa.attn_get_device_status() == 0
+    assert all(_intact(b[0]) for b in bufs), "a store escaped a gradient tensor"
+    to = lambda t: t.float().cpu().numpy()
+    return {"dq": to(dq), "dk": to(dk), "dv": to(dv), "o": to(o)}
+
+
+EDGE_N = [1, 2, 63, 64, 65, 127, 128, 129, 196, 255, 256, 257, 1000]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("n", EDGE_N)
+def test_bwd_edge_sizes(n, d):
+    inp = make_qkv(1, 3, n, d, seed=9000 + n + d)
+    scale = 1.0 / math.sqrt(d)
+    got = run_fwd_bwd(inp, scale)
+    ref = oracle.bwd(inp["q"], inp["k"], inp["v"], inp["do"], scale)
+    for name in ("dq", "dk", "dv"):
+        if n == 1 and name in ("dq", "dk"):   # exactly zero: compare absolutely
+            assert np.abs(got[name]).max() <= 1e-6
+            continue
+        check_grad(name, got[name], ref[name], f"N={n} d={d}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_bwd_wide_logits_and_scale(d):
+    inp = make_qkv(2, 2, 700, d, seed=21, qk_std=2.0)
+    for scale in (1.0 / math.sqrt(d), 0.37):
+        got = run_fwd_bwd(inp, scale)
+        ref = oracle.bwd(inp["q"], inp["k"], inp["v"], inp["do"], scale)
+        for name in ("dq", "dk", "dv"):
+            check_grad(name, got[name], ref[name], f"d={d} scale={scale}")
+
+
+def test_bwd_identities_on_gpu():
+    """sum_j dK_j = 0 and sum_j dV_j = sum_i dO_i hold for the GPU gradients too."""
+    inp = make_qkv(2, 3, 517, 128, seed=22)
+    got = run_fwd_bwd(inp, 1.0 / math.sqrt(128))
+    dk_sum = got["dk"].sum(axis=2)
+    assert np.abs(dk_sum).max() <= 2e-2 * np.abs(got["dk"]).max() * math.sqrt(517)
+    dv_sum = got["dv"].sum(axis=2)
+    do_sum = inp["do"].double().sum(dim=2).numpy()
+    assert np.abs(dv_sum - do_sum).max() <= 1e-2 * max(np.abs(do_sum).max(), 1.0)
+
+
+def test_bwd_dk_dv_deterministic():
+    inp = make_qkv(1, 4, 777, 64, seed=23)
+    a = run_fwd_bwd(inp, 0.125)
+    b = run_fwd_bwd(inp, 0.125)
+    np.testing.assert_array_equal(a["dk"], b["dk"])
+    np.testing.assert_array_equal(a["dv"], b["dv"])
+    check_grad("dq", a["dq"], b["dq"].astype(np.float64), "repeat")
+
+
+def test_bwd_workspace_errors():
+    inp = make_qkv(1, 2, 100, 64, seed=24)
+    q, k, v, do = (inp[x].cuda() for x in ("q", "k", "v", "do"))
+    o, lse = sa.forward(q, k, v)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    need = sa.attn_bwd_workspace_size(1, 2, 100, 64)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    with pytest.raises(sa.AttnError) as e:
+        sa.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, need - 16, 1, 2, 100, 64, 0.125)
+    assert e.value.code == 6
+    with pytest.raises(sa.AttnError) as e:
+        sa.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, ws[16:], need - 16, 1, 2, 100, 64, 0.125)
+    assert e.value.code == 6
+    with pytest.raises(sa.AttnError) as e:   # an output aliasing an input
+        sa.attn_bwd(q, k, v, o, do, lse, q, dk, dv, ws, need, 1, 2, 100, 64, 0.125)
+    assert e.value.code == 1
+
+
+def test_autograd_function():
+    inp = make_qkv(1, 2, 150, 64, seed=25)
+    q, k, v = (inp[x].cuda().requires_grad_(True) for x in ("q", "k", "v"))
+    o = sa.attention(q, k, v)
+    o.backward(inp["do"].cuda())
+    ref = oracle.bwd(inp["q"], inp["k"], inp["v"], inp["do"], 0.125)
+    for name, t in (("dq", q), ("dk", k), ("dv", v)):
+        check_grad(name, t.grad.float().cpu().numpy(), ref[name], "autograd")
+
+
+@pytest.mark.parametrize("name", ["vit_b16_batch", "vit_b_mhsa_block"])
+def test_bwd_workload_full(name):
+    w = WORKLOADS[name]
+    inp = make_workload_inputs(w)
+    got = run_fwd_bwd(inp, w.scale)
+    if name == "vit_b_mhsa_block":   # a spread of 24 of the 384 heads, every element
+        sel = np.linspace(0, w.bh - 1, 24).astype(int)
+        pick = lambda t: t.reshape(w.bh, w.N, w.d)[sel][None]
+        ref = oracle.bwd(*(pick(inp[x]) for x in ("q", "k", "v", "do")), w.scale)
+        got = {n_: pick(torch.from_numpy(got[n_])).numpy() for n_ in ("dq", "dk", "dv")}
+    else:
+        ref = oracle.bwd(inp["q"], inp["k"], inp["v"], inp["do"], w.scale)
+    for n_ in ("dq", "dk", "dv"):
+        check_grad(n_, got[n_], ref[n_], name)
+
+
+@pytest.mark.parametrize("name", ["vit_l_highres", "long_text"])
+def test_bwd_workload_sampled(name):
+    """Full-size workloads in the benchmark's launch configuration; sampled query and key rows
+    of some heads against the oracle's row-wise backward."""
+    w = WORKLOADS[name]
+    inp = make_workload_inputs(w)
+    got = run_fwd_bwd(inp, w.scale)
+    heads = [(0, 0), (w.B - 1, w.H - 1)] if name == "vit_l_highres" else [(w.B - 1, w.H // 2)]
+    rng = np.random.default_rng(2)
+    for (b, h) in heads:
+        qrows = np.unique(np.concatenate([[0, w.N - 1], rng.integers(0, w.N, 40)]))
+        krows = np.unique(np.concatenate([[0, w.N - 1], rng.integers(0, w.N, 40)]))
+        dq, dk, dv = oracle.bwd_rows(inp["q"][b, h], inp["k"][b, h], inp["v"][b, h],
+                                     inp["do"][b, h], qrows, krows, w.scale)
+        where = f"{name} head ({b},{h})"
+        check_grad("dq", got["dq"][b, h, qrows], dq, where)
+        check_grad("dk", got["dk"][b, h, krows], dk, where)
+        check_grad("dv", got["dv"][b, h, krows], dv, where)
+
+
+def test_wait_timeout_reports_status():
+    """A kernel wait that nobody satisfies gives up after its limit and the next status read
+    reports ATTN_ERR_TIMEOUT; the context stays usable."""
+    assert sa.attn_get_device_status() == 0
+    sa.attn_debug_wait_timeout(2000)
+    assert sa.attn_get_device_status() == 5
+    assert sa.attn_get_device_status() == 0
+    inp = make_qkv(1, 1, 64, 64, seed=26, with_do=False)
+    o, lse = sa.forward(inp["q"].cuda(), inp["k"].cuda(), inp["v"].cuda())
+    torch.cuda.synchronize()
+    assert sa.attn_get_device_status() == 0

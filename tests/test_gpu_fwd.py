@@ -1,0 +1,164 @@
+"""Forward parity: the CUDA path (through the C ABI) against the fp64 oracle, on the same
+seeded bf16 inputs."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import self_attention_gb300 as sa
+from self_attention_gb300.inputs import WORKLOADS, make_qkv, make_workload_inputs
+from _compare import check_lse, check_o
+
+pytestmark = pytest.mark.gpu
+
+GUARD = 16384  # elements of NaN canary on each side of every output
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from self_attention_gb300.build import build
+    sa.load_library(build())
+
+
+def _guarded(shape, dtype, dev="cuda"):
+    n = int(np.prod(shape))
+    buf = torch.full((n + 2 * GUARD,), float("nan"), dtype=dtype, device=dev)
+    return buf, buf[GUARD:GUARD + n].view(shape)
+
+
+def _guards_intact(buf):
+    g = torch.cat([buf[:GUARD], buf[-GUARD:]])
+    return bool(torch.isnan(g).all())
+
+
+def oracle_fwd(inp, scale):
+    """Oracle O, LSE and A = sum_j P_ij |V_j| (the oracle on |V|) for the O bound."""
+    o_ref, lse_ref = oracle.fwd(inp["q"], inp["k"], inp["v"], scale)
+    a_abs, _ = oracle.fwd(inp["q"], inp["k"], inp["v"].abs(), scale)
+    return o_ref, lse_ref, a_abs
+
+
+def run_fwd(inp, scale):
+    q, k, v = (inp[x].cuda() for x in ("q", "k", "v"))
+    B, H, N, D = q.shape
+    obuf, o = _guarded((B, H, N, D), torch.bfloat16)
+    lbuf, lse = _guarded((B, H, N), torch.float32)
+    sa.attn_fwd(q, k, v, o, lse, B, H, N, D, scale)
+    assert sa.attn_get_device_status() == 0
+    assert _guards_intact(obuf) and _guards_intact(lbuf), "a store escaped the output tensor"
+    return o.float().cpu().numpy(), lse.cpu().numpy()
+
+
+EDGE_N = [1, 2, 63, 64, 65, 127, 128, 129, 195, 196, 197, 255, 256, 257, 383, 1000]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("n", EDGE_N)
+def test_fwd_edge_sizes(n, d):
+    inp = make_qkv(1, 3, n, d, seed=7000 + n + d, with_do=False)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = run_fwd(inp, scale)
+    o_ref, lse_ref, a_abs = oracle_fwd(inp, scale)
+    check_o(o, o_ref, a_abs, f"N={n} d={d}")
+    check_lse(lse, lse_ref, f"N={n} d={d}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_fwd_wide_logits(d):
+    """Q, K ~ N(0, 2^2) as in the long-text workload: logits with standard deviation 4 move
+    the running maximum often, exercising the rescaling of O."""
+    inp = make_qkv(2, 2, 700, d, seed=11, qk_std=2.0, with_do=False)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = run_fwd(inp, scale)
+    o_ref, lse_ref, a_abs = oracle_fwd(inp, scale)
+    check_o(o, o_ref, a_abs, f"d={d}")
+    check_lse(lse, lse_ref, f"d={d}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_fwd_other_scale(d):
+    inp = make_qkv(1, 3, 333, d, seed=12, with_do=False)
+    o, lse = run_fwd(inp, 0.37)
+    o_ref, lse_ref, a_abs = oracle_fwd(inp, 0.37)
+    check_o(o, o_ref, a_abs, f"d={d} scale=0.37")
+    check_lse(lse, lse_ref, f"d={d} scale=0.37")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_fwd_extreme_logits(d):
+    """Logits with standard deviation 8 (beyond every workload): a few keys carry almost all
+    the weight, where the bf16 rounding of P dominates the error."""
+    inp = make_qkv(2, 2, 700, d, seed=13, qk_std=2.0 * math.sqrt(2.0), with_do=False)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = run_fwd(inp, scale)
+    o_ref, lse_ref, a_abs = oracle_fwd(inp, scale)
+    check_o(o, o_ref, a_abs, f"d={d} extreme")
+    check_lse(lse, lse_ref, f"d={d} extreme")
+
+
+def test_fwd_deterministic():
+    inp = make_qkv(2, 4, 517, 128, seed=5, with_do=False)
+    a = run_fwd(inp, 0.088)
+    b = run_fwd(inp, 0.088)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
+def test_fwd_invariants_on_gpu():
+    """Q = 0 gives mean(V) and LSE = log N; permuting K/V rows jointly leaves O unchanged."""
+    inp = make_qkv(1, 2, 300, 64, seed=3, with_do=False)
+    z = dict(inp, q=torch.zeros_like(inp["q"]))
+    o, lse = run_fwd(z, 0.125)
+    mean_v = inp["v"].double().mean(dim=2, keepdim=True).expand_as(inp["v"]).numpy()
+    mean_abs_v = inp["v"].double().abs().mean(dim=2, keepdim=True).expand_as(inp["v"]).numpy()
+    check_o(o, mean_v, mean_abs_v, "Q=0")
+    np.testing.assert_allclose(lse, math.log(300), rtol=0, atol=1e-5)
+    perm = torch.randperm(300, generator=torch.Generator().manual_seed(0))
+    p = dict(inp, k=inp["k"][:, :, perm].contiguous(), v=inp["v"][:, :, perm].contiguous())
+    o1, l1 = run_fwd(inp, 0.125)
+    o2, l2 = run_fwd(p, 0.125)
+    np.testing.assert_allclose(o2, o1, rtol=0, atol=2 ** -7)
+    np.testing.assert_allclose(l2, l1, rtol=0, atol=1e-5)
+
+
+def _sampled_check(w, inp, o, lse, heads, rows_per_head, seed):
+    rng = np.random.default_rng(seed)
+    q, k, v = inp["q"], inp["k"], inp["v"]
+    for (b, h) in heads:
+        rows = np.unique(np.concatenate([[0, w.N - 1], rng.integers(0, w.N, rows_per_head)]))
+        o_ref, lse_ref = oracle.fwd_rows(q[b, h], k[b, h], v[b, h], rows, w.scale)
+        a_abs, _ = oracle.fwd_rows(q[b, h], k[b, h], v[b, h].abs(), rows, w.scale)
+        check_o(o[b, h, rows], o_ref, a_abs, f"{w.name} head ({b},{h})")
+        check_lse(lse[b, h, rows], lse_ref, f"{w.name} head ({b},{h})")
+
+
+@pytest.mark.parametrize("name", ["vit_b16_single", "vit_b16_batch", "vit_b_mhsa_block"])
+def test_fwd_workload_full(name):
+    """Small workloads: every output element against the oracle."""
+    w = WORKLOADS[name]
+    inp = make_workload_inputs(w)
+    o, lse = run_fwd(inp, w.scale)
+    if name == "vit_b_mhsa_block":   # 384 heads of N=576: check a spread of 24 heads in full
+        sel = np.linspace(0, w.bh - 1, 24).astype(int)
+        pick = lambda t: t.reshape(w.bh, w.N, w.d)[sel].reshape(1, -1, w.N, w.d)
+        inp = {x: pick(inp[x]) for x in ("q", "k", "v")}
+        o = o.reshape(w.bh, w.N, w.d)[sel][None]
+        lse = lse.reshape(w.bh, w.N)[sel][None]
+    o_ref, lse_ref, a_abs = oracle_fwd(inp, w.scale)
+    check_o(o, o_ref, a_abs, name)
+    check_lse(lse, lse_ref, name)
+
+
+@pytest.mark.parametrize("name", ["vit_l_highres", "long_text"])
+def test_fwd_workload_sampled(name):
+    """Full-size workloads in the benchmark's launch configuration; sampled rows of a few
+    heads against the oracle (each row of the definition is independent)."""
+    w = WORKLOADS[name]
+    inp = make_workload_inputs(w)
+    o, lse = run_fwd(inp, w.scale)
+    heads = [(0, 0), (w.B - 1, w.H - 1), (w.B // 2, w.H // 3)]
+    _sampled_check(w, inp, o, lse, heads, rows_per_head=24, seed=1)
