@@ -249,10 +249,10 @@ def run_ours(args, world, rank, local):
         sa.attn_fwd(q, k, v, o, lse, B, H, N, D, scale, stream)
         if ev:
             ev[1].record(stream)
-        sa.attn_bwd_preprocess(o, do, ws, ws_bytes, B, H, N, D, stream)
+        sa.attn_bwd_preprocess(o, do, lse, ws, ws_bytes, B, H, N, D, stream)
         if ev:
             ev[2].record(stream)
-        sa.attn_bwd_main(q, k, v, do, lse, dk, dv, ws, ws_bytes, B, H, N, D, scale, stream)
+        sa.attn_bwd_main(q, k, v, do, dk, dv, ws, ws_bytes, B, H, N, D, scale, stream)
         if ev:
             ev[3].record(stream)
         sa.attn_bwd_dq_convert(ws, ws_bytes, dq, B, H, N, D, scale, stream)

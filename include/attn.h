@@ -62,9 +62,10 @@ attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float
                      int H, int N, int d_k, float scale, cudaStream_t stream);
 
 /*
- * Bytes of device workspace attn_bwd() needs for these sizes: D = rowsum(dO o O) ([B,H,N]
- * fp32) and an fp32 dQ accumulator ([B,H,N,d_k]), each 256-byte aligned.  Returns 0 if the
- * sizes are unsupported.
+ * Bytes of device workspace attn_bwd() needs for these sizes: two per-row fp32 vectors
+ * (D = rowsum(dO o O) and lse * log2(e), [B,H] x N rounded up to 64) and an fp32 dQ
+ * accumulator ([B,H,N,d_k]), each region 256-byte aligned.  Returns 0 if the sizes are
+ * unsupported.
  */
 size_t attn_bwd_workspace_size(int B, int H, int N, int d_k);
 
@@ -92,20 +93,20 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
  * separately.  Run on one stream, in this order, with the same sizes, scale and workspace,
  * they produce exactly what attn_bwd() produces.
  *
- * attn_bwd_preprocess: D_i = sum_c dO_ic O_ic into the workspace's D vector, and zeroes the
- *   workspace's fp32 dQ accumulator.  Reads o and dout.
- * attn_bwd_main: for every 128-key tile, recomputes P from q, k and lse, and writes dk
- *   (= scale * dS^T Q) and dv (= P^T dO); adds dS K into the dQ accumulator.  Reads q, k, v,
- *   dout, lse and the workspace's D vector.
+ * attn_bwd_preprocess: reads o, dout and lse; writes into the workspace D_i = sum_c dO_ic O_ic
+ *   and lse_i * log2(e) (rows padded to a multiple of 64; padding rows get D = 0 and +inf,
+ *   i.e. zero probability), and zeroes the workspace's fp32 dQ accumulator.
+ * attn_bwd_main: for every 128-key tile, recomputes P = 2^(scale log2(e) q.k - lse log2(e))
+ *   from q, k and the workspace, writes dk (= scale * dS^T Q) and dv (= P^T dO), and adds
+ *   dS K into the dQ accumulator.  Reads q, k, v, dout and the workspace.
  * attn_bwd_dq_convert: dq = bf16(scale * accumulator).
  */
-attn_status attn_bwd_preprocess(const void *o, const void *dout, void *workspace,
-                                size_t workspace_bytes, int B, int H, int N, int d_k,
-                                cudaStream_t stream);
+attn_status attn_bwd_preprocess(const void *o, const void *dout, const float *lse,
+                                void *workspace, size_t workspace_bytes, int B, int H, int N,
+                                int d_k, cudaStream_t stream);
 attn_status attn_bwd_main(const void *q, const void *k, const void *v, const void *dout,
-                          const float *lse, void *dk, void *dv, void *workspace,
-                          size_t workspace_bytes, int B, int H, int N, int d_k, float scale,
-                          cudaStream_t stream);
+                          void *dk, void *dv, void *workspace, size_t workspace_bytes, int B,
+                          int H, int N, int d_k, float scale, cudaStream_t stream);
 attn_status attn_bwd_dq_convert(void *workspace, size_t workspace_bytes, void *dq, int B, int H,
                                 int N, int d_k, float scale, cudaStream_t stream);
 

@@ -68,9 +68,9 @@ def load_library(path: str = LIB_PATH):
     lib.attn_bwd_workspace_size.restype = _SZ
     lib.attn_bwd.argtypes = [_VP] * 10 + [_SZ] + [_I] * 4 + [_F, _VP]
     lib.attn_bwd.restype = _I
-    lib.attn_bwd_preprocess.argtypes = [_VP] * 3 + [_SZ] + [_I] * 4 + [_VP]
+    lib.attn_bwd_preprocess.argtypes = [_VP] * 4 + [_SZ] + [_I] * 4 + [_VP]
     lib.attn_bwd_preprocess.restype = _I
-    lib.attn_bwd_main.argtypes = [_VP] * 8 + [_SZ] + [_I] * 4 + [_F, _VP]
+    lib.attn_bwd_main.argtypes = [_VP] * 7 + [_SZ] + [_I] * 4 + [_F, _VP]
     lib.attn_bwd_main.restype = _I
     lib.attn_bwd_dq_convert.argtypes = [_VP, _SZ, _VP] + [_I] * 4 + [_F, _VP]
     lib.attn_bwd_dq_convert.restype = _I
@@ -135,18 +135,18 @@ def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes: int,
                                    _stream(stream)), "attn_bwd")
 
 
-def attn_bwd_preprocess(o, dout, workspace, workspace_bytes: int, B: int, H: int, N: int,
+def attn_bwd_preprocess(o, dout, lse, workspace, workspace_bytes: int, B: int, H: int, N: int,
                         d_k: int, stream=None):
-    _raise(load_library().attn_bwd_preprocess(_ptr(o), _ptr(dout), _ptr(workspace),
+    _raise(load_library().attn_bwd_preprocess(_ptr(o), _ptr(dout), _ptr(lse), _ptr(workspace),
                                               int(workspace_bytes), B, H, N, d_k, _stream(stream)),
            "attn_bwd_preprocess")
 
 
-def attn_bwd_main(q, k, v, dout, lse, dk, dv, workspace, workspace_bytes: int, B: int, H: int,
-                  N: int, d_k: int, scale: float, stream=None):
-    _raise(load_library().attn_bwd_main(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(lse), _ptr(dk),
-                                        _ptr(dv), _ptr(workspace), int(workspace_bytes), B, H, N,
-                                        d_k, float(scale), _stream(stream)), "attn_bwd_main")
+def attn_bwd_main(q, k, v, dout, dk, dv, workspace, workspace_bytes: int, B: int, H: int, N: int,
+                  d_k: int, scale: float, stream=None):
+    _raise(load_library().attn_bwd_main(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dk), _ptr(dv),
+                                        _ptr(workspace), int(workspace_bytes), B, H, N, d_k,
+                                        float(scale), _stream(stream)), "attn_bwd_main")
 
 
 def attn_bwd_dq_convert(workspace, workspace_bytes: int, dq, B: int, H: int, N: int, d_k: int,

@@ -35,6 +35,12 @@ attn_status fail(const char *what, cudaError_t e)
                   cudaGetErrorString(e));
     return ATTN_ERR_LAUNCH;
 }
+
+attn_status fail_driver(const char *what, CUresult r)
+{
+    std::snprintf(t_last_error, sizeof t_last_error, "%s: CUresult %d", what, (int)r);
+    return ATTN_ERR_LAUNCH;
+}
 DeviceState g_devices[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -45,6 +51,10 @@ attn_status device_state(DeviceState **out)
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return fail("cudaGetDevice", e);
     if (dev < 0 || dev >= kMaxDevices) return fail("cudaGetDevice", cudaErrorInvalidDevice);
+    // Bind the device's primary context to this host thread: the driver calls made below
+    // (tensor-map encoding) need a current context, and a thread that has not used this
+    // library's runtime before (e.g. an autograd worker) may have none.
+    if ((e = cudaSetDevice(dev)) != cudaSuccess) return fail("cudaSetDevice", e);
     std::lock_guard<std::mutex> lock(g_mutex);
     DeviceState &s = g_devices[dev];
     if (!s.ready) {
@@ -78,7 +88,7 @@ attn_status device_state(DeviceState **out)
 
 // 3-D map over [BH, N, d] bf16 (innermost first: d, N, BH), boxes of 64 x box_rows x 1 with
 // the 128-byte swizzle.  Rows past N (or past a head) read as zeros.
-bool make_map(CUtensorMap *m, const void *base, int bh, int n, int d, int box_rows)
+CUresult make_map(CUtensorMap *m, const void *base, int bh, int n, int d, int box_rows)
 {
     cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)n, (cuuint64_t)bh};
     cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)n * d * 2};
@@ -87,7 +97,7 @@ bool make_map(CUtensorMap *m, const void *base, int bh, int n, int d, int box_ro
     return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
                     box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -142,9 +152,11 @@ extern "C" attn_status attn_fwd(const void *q, const void *k, const void *v, voi
     if ((st = device_state(&dev)) != ATTN_OK) return st;
     FwdArgs a;
     std::memset(&a, 0, sizeof a);
-    if (!make_map(&a.tm_q, q, (int)bh, N, d_k, 128) || !make_map(&a.tm_k, k, (int)bh, N, d_k, 128) ||
-        !make_map(&a.tm_v, v, (int)bh, N, d_k, 128))
-        return fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
+    CUresult r;
+    if ((r = make_map(&a.tm_q, q, (int)bh, N, d_k, 128)) != CUDA_SUCCESS ||
+        (r = make_map(&a.tm_k, k, (int)bh, N, d_k, 128)) != CUDA_SUCCESS ||
+        (r = make_map(&a.tm_v, v, (int)bh, N, d_k, 128)) != CUDA_SUCCESS)
+        return fail_driver("cuTensorMapEncodeTiled", r);
     a.o = o;
     a.lse = lse;
     a.bh = (int)bh;
@@ -158,52 +170,74 @@ extern "C" attn_status attn_fwd(const void *q, const void *k, const void *v, voi
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+namespace {
+
+// Workspace layout (every region 256-byte aligned), with N_pad = N rounded up to 64:
+//   D     [BH][N_pad] fp32   rowsum(dO o O); 0 in the padding
+//   LSE2  [BH][N_pad] fp32   lse * log2(e); +inf in the padding (probabilities there are 0)
+//   dQacc [BH][N][d]  fp32   dQ accumulator (unscaled)
+struct WorkspaceLayout {
+    size_t d_off, lse2_off, acc_off, total;
+};
+
+WorkspaceLayout workspace_layout(long long bh, int N, int d_k)
+{
+    const size_t n_pad = ((size_t)N + 63) / 64 * 64;
+    WorkspaceLayout w;
+    w.d_off = 0;
+    w.lse2_off = align256((size_t)bh * n_pad * 4);
+    w.acc_off = w.lse2_off + align256((size_t)bh * n_pad * 4);
+    w.total = w.acc_off + align256((size_t)bh * N * d_k * 4);
+    return w;
+}
+
+}  // namespace
+
 extern "C" size_t attn_bwd_workspace_size(int B, int H, int N, int d_k)
 {
     if (check_sizes(B, H, N, d_k, 1.0f) != ATTN_OK) return 0;
-    const size_t rows = (size_t)B * H * N;
-    return align256(rows * 4) + align256(rows * d_k * 4);
+    return workspace_layout((long long)B * H, N, d_k).total;
 }
 
 namespace {
 
-// Validates what a backward phase needs and fills `a`.  Null pointers mark operands the phase
-// does not use (they are neither checked nor mapped); the workspace is always required.
-attn_status prepare_bwd(BwdArgs &a, const void *q, const void *k, const void *v, const void *o,
-                        const void *dout, const float *lse, void *dq, void *dk, void *dv,
-                        void *workspace, size_t workspace_bytes, int B, int H, int N, int d_k,
-                        float scale, bool need_qkv, bool need_o, bool need_dq)
+enum Phase : unsigned { kPre = 1, kMain = 2, kConv = 4 };
+
+// Validates what the requested backward phases need and fills `a`.  Operands a phase does
+// not use may be null; they are neither checked nor mapped.  The workspace is always needed.
+attn_status prepare_bwd(BwdArgs &a, unsigned phases, const void *q, const void *k, const void *v,
+                        const void *o, const void *dout, const float *lse, void *dq, void *dk,
+                        void *dv, void *workspace, size_t workspace_bytes, int B, int H, int N,
+                        int d_k, float scale)
 {
     attn_status st = check_sizes(B, H, N, d_k, scale);
     if (st != ATTN_OK) return st;
-    const void *ins_needed[6] = {need_qkv ? q : nullptr, need_qkv ? k : nullptr,
-                                 need_qkv ? v : nullptr, need_o ? o : nullptr, dout,
-                                 need_qkv ? static_cast<const void *>(lse) : nullptr};
-    if ((need_qkv && (!q || !k || !v || !lse || !dk || !dv)) || (need_o && !o) ||
-        ((need_qkv || need_o) && !dout) || (need_dq && !dq))
+    const bool pre = phases & kPre, main = phases & kMain, conv = phases & kConv;
+    if ((pre && (!o || !dout || !lse)) || (main && (!q || !k || !v || !dout || !dk || !dv)) ||
+        (conv && !dq))
         return ATTN_ERR_INVALID_ARG;
-    for (const void *p : {q, k, v, o, dout, static_cast<const void *>(lse),
-                          static_cast<const void *>(dq), static_cast<const void *>(dk),
-                          static_cast<const void *>(dv)})
-        if (p && !aligned16(p)) return ATTN_ERR_MISALIGNED;
-    const size_t need = attn_bwd_workspace_size(B, H, N, d_k);
-    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
-        return ATTN_ERR_WORKSPACE;
+    const void *all[9] = {q, k, v, o, dout, lse, dq, dk, dv};
+    const bool used[9] = {main, main, main, pre, pre || main, pre, conv, main, main};
+    for (int i = 0; i < 9; ++i)
+        if (used[i] && !aligned16(all[i])) return ATTN_ERR_MISALIGNED;
     const long long bh = (long long)B * H;
+    const WorkspaceLayout wl = workspace_layout(bh, N, d_k);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < wl.total)
+        return ATTN_ERR_WORKSPACE;
     const size_t tbytes = (size_t)bh * N * d_k * 2, lbytes = (size_t)bh * N * 4;
+    // inputs: q k v o dout lse ; outputs: workspace dq dk dv
     Range outs[4];
     int n_out = 0;
-    outs[n_out++] = span(workspace, need);
-    if (need_qkv) {
+    outs[n_out++] = span(workspace, wl.total);
+    if (conv) outs[n_out++] = span(dq, tbytes);
+    if (main) {
         outs[n_out++] = span(dk, tbytes);
         outs[n_out++] = span(dv, tbytes);
     }
-    if (need_dq) outs[n_out++] = span(dq, tbytes);
     for (int i = 0; i < n_out; ++i) {
-        for (int j = 0; j < 6; ++j) {
-            if (!ins_needed[j]) continue;
-            if (overlap(span(ins_needed[j], j == 5 ? lbytes : tbytes), outs[i])) return ATTN_ERR_INVALID_ARG;
-        }
+        for (int j = 0; j < 6; ++j)
+            if (used[j] && overlap(span(all[j], j == 5 ? lbytes : tbytes), outs[i]))
+                return ATTN_ERR_INVALID_ARG;
         for (int j = i + 1; j < n_out; ++j)
             if (overlap(outs[i], outs[j])) return ATTN_ERR_INVALID_ARG;
     }
@@ -211,20 +245,25 @@ attn_status prepare_bwd(BwdArgs &a, const void *q, const void *k, const void *v,
     DeviceState *dev = nullptr;
     if ((st = device_state(&dev)) != ATTN_OK) return st;
     std::memset(&a, 0, sizeof a);
-    if (need_qkv && (!make_map(&a.tm_q, q, (int)bh, N, d_k, 64) || !make_map(&a.tm_k, k, (int)bh, N, d_k, 128) ||
-                     !make_map(&a.tm_v, v, (int)bh, N, d_k, 128) ||
-                     !make_map(&a.tm_do, dout, (int)bh, N, d_k, 64)))
-        return fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
+    CUresult r;
+    if (main && ((r = make_map(&a.tm_q, q, (int)bh, N, d_k, 64)) != CUDA_SUCCESS ||
+                 (r = make_map(&a.tm_k, k, (int)bh, N, d_k, 128)) != CUDA_SUCCESS ||
+                 (r = make_map(&a.tm_v, v, (int)bh, N, d_k, 128)) != CUDA_SUCCESS ||
+                 (r = make_map(&a.tm_do, dout, (int)bh, N, d_k, 64)) != CUDA_SUCCESS))
+        return fail_driver("cuTensorMapEncodeTiled", r);
+    char *ws = static_cast<char *>(workspace);
     a.o = o;
     a.dout = dout;
     a.lse = lse;
     a.dq = dq;
     a.dk = dk;
     a.dv = dv;
-    a.dvec = static_cast<float *>(workspace);
-    a.dq_acc = reinterpret_cast<float *>(static_cast<char *>(workspace) + align256((size_t)bh * N * 4));
+    a.dvec = reinterpret_cast<float *>(ws + wl.d_off);
+    a.lse2 = reinterpret_cast<float *>(ws + wl.lse2_off);
+    a.dq_acc = reinterpret_cast<float *>(ws + wl.acc_off);
     a.bh = (int)bh;
     a.n = N;
+    a.n_pad = (N + 63) / 64 * 64;
     a.d = d_k;
     a.scale = scale;
     a.status = dev->status;
@@ -233,27 +272,25 @@ attn_status prepare_bwd(BwdArgs &a, const void *q, const void *k, const void *v,
 
 }  // namespace
 
-extern "C" attn_status attn_bwd_preprocess(const void *o, const void *dout, void *workspace,
-                                           size_t workspace_bytes, int B, int H, int N, int d_k,
-                                           cudaStream_t stream)
+extern "C" attn_status attn_bwd_preprocess(const void *o, const void *dout, const float *lse,
+                                           void *workspace, size_t workspace_bytes, int B, int H,
+                                           int N, int d_k, cudaStream_t stream)
 {
     BwdArgs a;
-    attn_status st = prepare_bwd(a, nullptr, nullptr, nullptr, o, dout, nullptr, nullptr, nullptr,
-                                 nullptr, workspace, workspace_bytes, B, H, N, d_k, 1.0f, false,
-                                 true, false);
+    attn_status st = prepare_bwd(a, kPre, nullptr, nullptr, nullptr, o, dout, lse, nullptr, nullptr,
+                                 nullptr, workspace, workspace_bytes, B, H, N, d_k, 1.0f);
     if (st != ATTN_OK) return st;
     const cudaError_t e = launch_bwd_preprocess(a, stream);
     return e == cudaSuccess ? ATTN_OK : fail("attn_bwd_preprocess launch", e);
 }
 
 extern "C" attn_status attn_bwd_main(const void *q, const void *k, const void *v, const void *dout,
-                                     const float *lse, void *dk, void *dv, void *workspace,
-                                     size_t workspace_bytes, int B, int H, int N, int d_k,
-                                     float scale, cudaStream_t stream)
+                                     void *dk, void *dv, void *workspace, size_t workspace_bytes,
+                                     int B, int H, int N, int d_k, float scale, cudaStream_t stream)
 {
     BwdArgs a;
-    attn_status st = prepare_bwd(a, q, k, v, nullptr, dout, lse, nullptr, dk, dv, workspace,
-                                 workspace_bytes, B, H, N, d_k, scale, true, false, false);
+    attn_status st = prepare_bwd(a, kMain, q, k, v, nullptr, dout, nullptr, nullptr, dk, dv,
+                                 workspace, workspace_bytes, B, H, N, d_k, scale);
     if (st != ATTN_OK) return st;
     const cudaError_t e = launch_bwd_main(a, stream);
     return e == cudaSuccess ? ATTN_OK : fail("attn_bwd_main launch", e);
@@ -264,9 +301,8 @@ extern "C" attn_status attn_bwd_dq_convert(void *workspace, size_t workspace_byt
                                            cudaStream_t stream)
 {
     BwdArgs a;
-    attn_status st = prepare_bwd(a, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, dq,
-                                 nullptr, nullptr, workspace, workspace_bytes, B, H, N, d_k, scale,
-                                 false, false, true);
+    attn_status st = prepare_bwd(a, kConv, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, dq,
+                                 nullptr, nullptr, workspace, workspace_bytes, B, H, N, d_k, scale);
     if (st != ATTN_OK) return st;
     const cudaError_t e = launch_bwd_convert(a, stream);
     return e == cudaSuccess ? ATTN_OK : fail("attn_bwd_dq_convert launch", e);
@@ -278,8 +314,8 @@ extern "C" attn_status attn_bwd(const void *q, const void *k, const void *v, con
                                 int d_k, float scale, cudaStream_t stream)
 {
     BwdArgs a;
-    attn_status st = prepare_bwd(a, q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes,
-                                 B, H, N, d_k, scale, true, true, true);
+    attn_status st = prepare_bwd(a, kPre | kMain | kConv, q, k, v, o, dout, lse, dq, dk, dv,
+                                 workspace, workspace_bytes, B, H, N, d_k, scale);
     if (st != ATTN_OK) return st;
     cudaError_t e = launch_bwd_preprocess(a, stream);
     if (e == cudaSuccess) e = launch_bwd_main(a, stream);

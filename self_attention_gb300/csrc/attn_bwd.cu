@@ -9,9 +9,11 @@
 //   dS = P o (dP - D),  dQ = scale * dS K,  dK = scale * dS^T Q.
 //
 // Three stream-ordered kernels:
-//   1. preprocess: D = rowsum(dO o O) (fp32) and zero the fp32 dQ accumulator.
+//   1. preprocess: D = rowsum(dO o O) and LSE2 = LSE log2 e (fp32, rows padded to a multiple
+//      of 64 with D = 0, LSE2 = +inf so that padded queries get zero probability), and zero
+//      the fp32 dQ accumulator.
 //   2. main: one CTA per 128-key tile j of one head, looping over all 64-row query tiles i.
-//        warp 8     TMA producer: K_j and V_j once; a ring of (Q_i, dO_i) tiles.
+//        warp 8     TMA producer: K_j and V_j once; a ring of (Q_i, dO_i, LSE2_i, D_i).
 //        warp 9     tcgen05 issuer, per query tile:
 //                     S^T = K_j Q_i^T, dP^T = V_j dO_i^T          (into TMEM, double-buffered)
 //                     dV += P^T dO_i  (P^T from TMEM), dK += dS^T Q_i, dQ_i^T = K_j^T dS^T
@@ -36,12 +38,15 @@ template <int D>
 struct BwdCfg {
     static constexpr int BN = 128;   // keys per CTA (TMEM lanes of S^T, dP^T, dK, dV)
     static constexpr int BM = 64;    // queries per inner tile
-    static constexpr int QST = (D == 64) ? 4 : 2;  // (Q, dO) ring depth
+    static constexpr int QST = (D == 64) ? 4 : 2;  // (Q, dO, LSE2, D) ring depth
     static constexpr int KV_BYTES = BN * D * 2;
     static constexpr int Q_BYTES = BM * D * 2;
+    // one ring stage: Q_i, dO_i (swizzled tiles), then LSE2_i and D_i (64 fp32 each), padded
+    // to keep every tile 1024-byte aligned
+    static constexpr int STAGE_BYTES = 2 * Q_BYTES + 1024;
     static constexpr int DS_BYTES = BN * BM * 2;
     static constexpr int DQ_BYTES = BM * D * 4;
-    static constexpr int SMEM_BYTES = 2 * KV_BYTES + QST * 2 * Q_BYTES + 2 * DS_BYTES + DQ_BYTES + 1024;
+    static constexpr int SMEM_BYTES = 2 * KV_BYTES + QST * STAGE_BYTES + 2 * DS_BYTES + DQ_BYTES + 1024;
     static constexpr int THREADS = 320;
     static constexpr uint32_t TM_DK = 0, TM_DV = D, TM_BUF = 2 * D;
     __host__ __device__ static constexpr uint32_t tm_s(int b) { return TM_BUF + b * 128; }
@@ -49,25 +54,31 @@ struct BwdCfg {
 };
 
 // ------------------------------------------------------------------ 1. preprocess
+// Over the padded rows (bh, i), i < n_pad:  D = sum_c dO_ic O_ic and LSE2 = lse log2(e) for
+// i < n; D = 0 and LSE2 = +inf in the padding.  Then zero the dQ accumulator.
 template <int D>
 __global__ void __launch_bounds__(256)
     bwd_preprocess_kernel(const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restrict__ dout,
-                          float *__restrict__ dvec, float *__restrict__ dq_acc, long long rows)
+                          const float *__restrict__ lse, float *__restrict__ dvec,
+                          float *__restrict__ lse2, float *__restrict__ dq_acc, int bh, int n,
+                          int n_pad)
 {
-    // D: one group of D/8 threads per row, 8 bf16 (16 bytes) per thread.
-    constexpr int TPR = D / 8;
+    constexpr int TPR = D / 8;  // threads per row, 8 bf16 (16 bytes) each
     const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const long long nthreads = (long long)gridDim.x * blockDim.x;
-    // The loop runs whole warps in step (nthreads is a multiple of 32), so the shuffles below
-    // always see every lane of the warp.
+    const long long rows = (long long)bh * n_pad;
+    // Whole warps run the same iterations (nthreads is a multiple of 32), so the shuffles
+    // below always see all 32 lanes.
     const long long total = rows * TPR;
     const long long bound = (total + 31) & ~31LL;
     for (long long t = tid; t < bound; t += nthreads) {
-        const bool ok = t < total;
-        const long long row = t / TPR;
+        const long long prow = t / TPR;
         const int part = (int)(t % TPR);
+        const int h = (int)(prow / n_pad), i = (int)(prow % n_pad);
+        const bool live = t < total && i < n;
+        const long long row = (long long)h * n + i;
         float acc = 0.f;
-        if (ok) {
+        if (live) {
             const uint4 a = *reinterpret_cast<const uint4 *>(o + row * D + part * 8);
             const uint4 b = *reinterpret_cast<const uint4 *>(dout + row * D + part * 8);
             const __nv_bfloat162 *a2 = reinterpret_cast<const __nv_bfloat162 *>(&a);
@@ -82,11 +93,13 @@ __global__ void __launch_bounds__(256)
         }
 #pragma unroll
         for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (ok && part == 0) dvec[row] = acc;
+        if (t < total && part == 0) {
+            dvec[prow] = acc;
+            lse2[prow] = i < n ? lse[row] * kLog2e : INFINITY;
+        }
     }
-    // zero the dQ accumulator (16 bytes per store)
     float4 *acc4 = reinterpret_cast<float4 *>(dq_acc);
-    const long long n4 = rows * D / 4;
+    const long long n4 = (long long)bh * n * D / 4;
     for (long long t = tid; t < n4; t += nthreads) acc4[t] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
@@ -114,9 +127,9 @@ template <int D>
 __global__ void __launch_bounds__(320, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                    const float *__restrict__ lse, const float *__restrict__ dvec,
+                    const float *__restrict__ lse2, const float *__restrict__ dvec,
                     float *__restrict__ dq_acc, __nv_bfloat16 *__restrict__ dk,
-                    __nv_bfloat16 *__restrict__ dv, int n, int n_kvblocks, float scale,
+                    __nv_bfloat16 *__restrict__ dv, int n, int n_pad, int n_kvblocks, float scale,
                     int *status)
 {
     using C = BwdCfg<D>;
@@ -124,14 +137,13 @@ __global__ void __launch_bounds__(320, 1)
     uint8_t *smem = align1024(smem_raw);
     uint8_t *sK = smem;
     uint8_t *sV = sK + C::KV_BYTES;
-    uint8_t *sQ = sV + C::KV_BYTES;                 // QST stages of {Q_i, dO_i}
-    uint8_t *sDS = sQ + C::QST * 2 * C::Q_BYTES;    // two dS^T tiles
+    uint8_t *sQ = sV + C::KV_BYTES;                 // QST stages of {Q_i, dO_i, LSE2_i, D_i}
+    uint8_t *sDS = sQ + C::QST * C::STAGE_BYTES;    // two dS^T tiles
     float *sDQ = reinterpret_cast<float *>(sDS + 2 * C::DS_BYTES);  // dQ_i staging [BM][D]
 
     __shared__ uint64_t bar_kv, bar_qf[C::QST], bar_qe[C::QST];
     __shared__ uint64_t bar_sdp[2], bar_ds_full[2], bar_ds_empty[2], bar_dq_full[2], bar_dq_empty[2];
     __shared__ uint64_t bar_dkv, bar_done;
-    __shared__ float sLSE[2][C::BM], sDv[2][C::BM];
     __shared__ uint32_t tmem_sh;
     __shared__ int abort_sh;
 
@@ -184,13 +196,16 @@ __global__ void __launch_bounds__(320, 1)
                 const int s = it % C::QST;
                 const uint32_t ph = (it / C::QST) & 1;
                 wait_bounded(&bar_qe[s], ph ^ 1, g);
-                ptx::mbar_arrive_expect_tx(&bar_qf[s], 2 * C::Q_BYTES);
-                uint8_t *dq_tile = sQ + s * 2 * C::Q_BYTES;
+                ptx::mbar_arrive_expect_tx(&bar_qf[s], 2 * C::Q_BYTES + 2 * C::BM * 4);
+                uint8_t *stage = sQ + s * C::STAGE_BYTES;
                 for (int h = 0; h < D / 64; ++h) {
-                    ptx::tma_load_3d(dq_tile + h * C::BM * 128, &tm_q, &bar_qf[s], h * 64, it * C::BM, bh);
-                    ptx::tma_load_3d(dq_tile + C::Q_BYTES + h * C::BM * 128, &tm_do, &bar_qf[s],
+                    ptx::tma_load_3d(stage + h * C::BM * 128, &tm_q, &bar_qf[s], h * 64, it * C::BM, bh);
+                    ptx::tma_load_3d(stage + C::Q_BYTES + h * C::BM * 128, &tm_do, &bar_qf[s],
                                      h * 64, it * C::BM, bh);
                 }
+                const size_t rowvec = (size_t)bh * n_pad + (size_t)it * C::BM;
+                ptx::bulk_load(stage + 2 * C::Q_BYTES, lse2 + rowvec, C::BM * 4, &bar_qf[s]);
+                ptx::bulk_load(stage + 2 * C::Q_BYTES + C::BM * 4, dvec + rowvec, C::BM * 4, &bar_qf[s]);
             }
             wait_bounded(&bar_kv, 0, g);
             for (int it = (nq > C::QST ? nq - C::QST : 0); it < nq; ++it)
@@ -204,8 +219,8 @@ __global__ void __launch_bounds__(320, 1)
             const uint32_t idDQ = ptx::idesc_bf16_f32(128, C::BM, true, true);
             const uint32_t k_base = ptx::smem_u32(sK), v_base = ptx::smem_u32(sV);
             const uint32_t q_base = ptx::smem_u32(sQ), ds_base = ptx::smem_u32(sDS);
-            auto qs = [&](int s) { return q_base + s * 2 * C::Q_BYTES; };
-            auto dos = [&](int s) { return q_base + s * 2 * C::Q_BYTES + C::Q_BYTES; };
+            auto qs = [&](int s) { return q_base + s * C::STAGE_BYTES; };
+            auto dos = [&](int s) { return q_base + s * C::STAGE_BYTES + C::Q_BYTES; };
             // S^T = K_j Q_i^T and dP^T = V_j dO_i^T: all four operands K-major over d.
             auto issue_sdp = [&](int s, int b) {
 #pragma unroll
@@ -277,47 +292,46 @@ __global__ void __launch_bounds__(320, 1)
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
         const float scale_log2 = scale * kLog2e;
         for (int it = 0; it < nq; ++it) {
-            const int b = it & 1;
+            const int b = it & 1, s = it % C::QST;
             const uint32_t ph = (it >> 1) & 1;
-            {   // this tile's LSE (log2 units) and D into shared memory
-                const int c = threadIdx.x & 63;
-                const int qi = it * C::BM + c;
-                if (threadIdx.x < 64)
-                    sLSE[b][c] = qi < n ? lse[(size_t)bh * n + qi] * kLog2e : INFINITY;
-                else
-                    sDv[b][c] = qi < n ? dvec[(size_t)bh * n + qi] : 0.f;
-            }
-            ptx::named_bar(1, 128);
+            // this query tile's LSE2 (+inf past N) and D (0 past N), loaded with the tile
+            const float *sl = reinterpret_cast<const float *>(sQ + s * C::STAGE_BYTES + 2 * C::Q_BYTES);
+            const float *sd = sl + C::BM;
             wait_bounded(&bar_sdp[b], ph, g);
+            wait_bounded(&bar_ds_empty[b], ph ^ 1, g);
             ptx::tc_fence_after();
-            uint32_t pp[32], dsp[32];
+            uint8_t *rowp = sDS + b * C::DS_BYTES + r * 128;
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-                uint32_t sv[32], dpv[32];
+                uint32_t sv[32], dpv[32], pp[16], dsp[16];
                 ptx::tmem_ld32(tmem + lane_off + C::tm_s(b) + half * 32, sv);
                 ptx::tmem_ld32(tmem + lane_off + C::tm_dp(b) + half * 32, dpv);
                 ptx::tmem_ld_wait();
                 reg_fence(sv);
                 reg_fence(dpv);
 #pragma unroll
-                for (int c = 0; c < 32; c += 2) {
-                    const int q = half * 32 + c;
-                    float p0 = ptx::ex2(fmaf(__uint_as_float(sv[c]), scale_log2, -sLSE[b][q]));
-                    float p1 = ptx::ex2(fmaf(__uint_as_float(sv[c + 1]), scale_log2, -sLSE[b][q + 1]));
-                    if (!key_ok) p0 = p1 = 0.f;
-                    const float ds0 = p0 * (__uint_as_float(dpv[c]) - sDv[b][q]);
-                    const float ds1 = p1 * (__uint_as_float(dpv[c + 1]) - sDv[b][q + 1]);
-                    pp[q >> 1] = ptx::pack_bf16x2(p0, p1);
-                    dsp[q >> 1] = ptx::pack_bf16x2(ds0, ds1);
-                }
-            }
-            ptx::tmem_st32(tmem + lane_off + C::tm_s(b), pp);
-            wait_bounded(&bar_ds_empty[b], ph ^ 1, g);
-            uint8_t *rowp = sDS + b * C::DS_BYTES + r * 128;
+                for (int c = 0; c < 32; c += 4) {
+                    const float4 l4 = *reinterpret_cast<const float4 *>(sl + half * 32 + c);
+                    const float4 d4 = *reinterpret_cast<const float4 *>(sd + half * 32 + c);
+                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+                    float p[4], ds[4];
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch)
-                *reinterpret_cast<uint4 *>(rowp + ((ch ^ (r & 7)) << 4)) =
-                    make_uint4(dsp[4 * ch], dsp[4 * ch + 1], dsp[4 * ch + 2], dsp[4 * ch + 3]);
+                    for (int e = 0; e < 4; ++e) {
+                        p[e] = ptx::ex2(fmaf(__uint_as_float(sv[c + e]), scale_log2, -lv[e]));
+                        if (!key_ok) p[e] = 0.f;
+                        ds[e] = p[e] * (__uint_as_float(dpv[c + e]) - dv4[e]);
+                    }
+                    pp[c / 2] = ptx::pack_bf16x2(p[0], p[1]);
+                    pp[c / 2 + 1] = ptx::pack_bf16x2(p[2], p[3]);
+                    dsp[c / 2] = ptx::pack_bf16x2(ds[0], ds[1]);
+                    dsp[c / 2 + 1] = ptx::pack_bf16x2(ds[2], ds[3]);
+                }
+                ptx::tmem_st16(tmem + lane_off + C::tm_s(b) + half * 16, pp);
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    *reinterpret_cast<uint4 *>(rowp + (((half * 4 + cc) ^ (r & 7)) << 4)) =
+                        make_uint4(dsp[4 * cc], dsp[4 * cc + 1], dsp[4 * cc + 2], dsp[4 * cc + 3]);
+            }
             ptx::tmem_st_wait();
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
@@ -359,22 +373,24 @@ __global__ void __launch_bounds__(320, 1)
             const int b = it & 1;
             wait_bounded(&bar_dq_full[b], (it >> 1) & 1, g);
             ptx::tc_fence_after();
-            uint32_t v[64];
+            uint32_t v0[32], v1[32];
             if ((warp - 4) * 32 < D) {
-                uint32_t (&v0)[32] = *reinterpret_cast<uint32_t (*)[32]>(&v[0]);
-                uint32_t (&v1)[32] = *reinterpret_cast<uint32_t (*)[32]>(&v[32]);
                 ptx::tmem_ld32(tmem + lane_off + C::tm_dp(b), v0);
                 ptx::tmem_ld32(tmem + lane_off + C::tm_dp(b) + 32, v1);
                 ptx::tmem_ld_wait();
-                reg_fence(v);
+                reg_fence(v0);
+                reg_fence(v1);
             }
             ptx::tc_fence_before();
             ptx::mbar_arrive(&bar_dq_empty[b]);
             if (leader) ptx::bulk_wait_group_read<0>();   // staging buffer free again
             ptx::named_bar(2, 128);
             if (r < D) {
+                const uint32_t base = opaque(ptx::smem_u32(sDQ) + r * 4);
 #pragma unroll
-                for (int c = 0; c < C::BM; ++c) sDQ[c * D + r] = __uint_as_float(v[c]);
+                for (int c = 0; c < 32; ++c) sts_f32(base + c * D * 4, __uint_as_float(v0[c]));
+#pragma unroll
+                for (int c = 0; c < 32; ++c) sts_f32(base + (32 + c) * D * 4, __uint_as_float(v1[c]));
             }
             ptx::fence_proxy_async_smem();
             ptx::named_bar(2, 128);
@@ -414,7 +430,7 @@ cudaError_t launch_preprocess_d(const BwdArgs &a, cudaStream_t stream)
 {
     bwd_preprocess_kernel<D><<<elementwise_blocks(), 256, 0, stream>>>(
         reinterpret_cast<const __nv_bfloat16 *>(a.o), reinterpret_cast<const __nv_bfloat16 *>(a.dout),
-        a.dvec, a.dq_acc, (long long)a.bh * a.n);
+        a.lse, a.dvec, a.lse2, a.dq_acc, a.bh, a.n, a.n_pad);
     return cudaGetLastError();
 }
 
@@ -428,9 +444,9 @@ cudaError_t launch_main_d(const BwdArgs &a, cudaStream_t stream)
     const int n_kvblocks = (a.n + C::BN - 1) / C::BN;
     const long long ctas = (long long)n_kvblocks * a.bh;
     bwd_main_kernel<D><<<(unsigned)ctas, C::THREADS, C::SMEM_BYTES, stream>>>(
-        a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse, a.dvec, a.dq_acc,
+        a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse2, a.dvec, a.dq_acc,
         reinterpret_cast<__nv_bfloat16 *>(a.dk), reinterpret_cast<__nv_bfloat16 *>(a.dv), a.n,
-        n_kvblocks, a.scale, a.status);
+        a.n_pad, n_kvblocks, a.scale, a.status);
     return cudaGetLastError();
 }
 

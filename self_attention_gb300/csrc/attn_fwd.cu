@@ -213,18 +213,12 @@ __global__ void __launch_bounds__(320, 1)
             wait_bounded(&bar_s[t], j & 1, g);
             ptx::tc_fence_after();
             uint32_t r[128];
-            {
-                uint32_t (&r0)[32] = *reinterpret_cast<uint32_t (*)[32]>(&r[0]);
-                uint32_t (&r1)[32] = *reinterpret_cast<uint32_t (*)[32]>(&r[32]);
-                uint32_t (&r2)[32] = *reinterpret_cast<uint32_t (*)[32]>(&r[64]);
-                uint32_t (&r3)[32] = *reinterpret_cast<uint32_t (*)[32]>(&r[96]);
-                ptx::tmem_ld32(tS + 0, r0);
-                ptx::tmem_ld32(tS + 32, r1);
-                ptx::tmem_ld32(tS + 64, r2);
-                ptx::tmem_ld32(tS + 96, r3);
-                ptx::tmem_ld_wait();
-                reg_fence(r);
-            }
+            ptx::tmem_ld32_at<0>(tS + 0, r);
+            ptx::tmem_ld32_at<32>(tS + 32, r);
+            ptx::tmem_ld32_at<64>(tS + 64, r);
+            ptx::tmem_ld32_at<96>(tS + 96, r);
+            ptx::tmem_ld_wait();
+            reg_fence(r);
             // keys >= n (only in the last tile) take no weight
             const int valid = n - j * C::BN;
             if (valid < C::BN) {
@@ -251,16 +245,18 @@ __global__ void __launch_bounds__(320, 1)
             }
             const float neg_m = -m_new;
             float sum[4] = {0.f, 0.f, 0.f, 0.f};
-            uint32_t pk0[32], pk1[32];
+            // P = 2^(x - m) as bf16 pairs into TMEM over S_t, 32 keys (16 columns) at a time
 #pragma unroll
-            for (int i = 0; i < 128; i += 2) {
-                const float p0 = ptx::ex2(fmaf(__uint_as_float(r[i]), scale_log2, neg_m));
-                const float p1 = ptx::ex2(fmaf(__uint_as_float(r[i + 1]), scale_log2, neg_m));
-                sum[(i >> 1) & 3] += p0 + p1;
-                if (i < 64)
-                    pk0[i >> 1] = ptx::pack_bf16x2(p0, p1);
-                else
-                    pk1[(i - 64) >> 1] = ptx::pack_bf16x2(p0, p1);
+            for (int ch = 0; ch < 4; ++ch) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    const float p0 = ptx::ex2(fmaf(__uint_as_float(r[ch * 32 + i]), scale_log2, neg_m));
+                    const float p1 = ptx::ex2(fmaf(__uint_as_float(r[ch * 32 + i + 1]), scale_log2, neg_m));
+                    sum[(i >> 1) & 3] += p0 + p1;
+                    pk[i >> 1] = ptx::pack_bf16x2(p0, p1);
+                }
+                ptx::tmem_st16(tS + ch * 16, pk);
             }
             l = l * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
             m = m_new;
@@ -276,8 +272,6 @@ __global__ void __launch_bounds__(320, 1)
                     ptx::tmem_st32(tO + c, ov);
                 }
             }
-            ptx::tmem_st32(tS + 0, pk0);
-            ptx::tmem_st32(tS + 32, pk1);
             ptx::tmem_st_wait();
             ptx::tc_fence_before();
             ptx::mbar_arrive(&bar_p[t]);

@@ -53,6 +53,20 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[N])
     for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
 }
 
+// Returns `x` through an opaque move, so that addresses derived from it are recomputed where
+// they are used instead of being hoisted out of a loop into dozens of live registers.
+__device__ __forceinline__ uint32_t opaque(uint32_t x)
+{
+    uint32_t y;
+    asm volatile("mov.b32 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+__device__ __forceinline__ void sts_f32(uint32_t addr, float v)
+{
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
 {
     return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));

@@ -107,6 +107,17 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void 
                  : "memory");
 }
 
+// Plain (non-tensor) bulk copy global -> shared, completion on an mbarrier; both addresses
+// 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint32_t bytes,
+                                          uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(smem_dst)),
+                 "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
 // Element-wise fp32 add of a contiguous shared-memory block into global memory (bulk copy
 // engine; both addresses 16-byte aligned, size a multiple of 16).
 __device__ __forceinline__ void bulk_reduce_add_f32(float *gdst, const void *smem_src,
@@ -247,6 +258,20 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
 
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
 {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : ATTN_R8(0), ATTN_R8(8), ATTN_R8(16), ATTN_R8(24)
+        : "r"(taddr));
+}
+
+// tcgen05.ld 32x32b.x32 into r[OFF .. OFF+32) of a larger register array.
+template <int OFF, int N>
+__device__ __forceinline__ void tmem_ld32_at(uint32_t taddr, uint32_t (&a)[N])
+{
+    static_assert(OFF + 32 <= N, "slice out of range");
+    uint32_t *r = a + OFF;
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
         "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"

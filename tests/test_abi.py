@@ -48,8 +48,9 @@ def test_status_strings(lib):
 
 def test_workspace_size(lib):
     a256 = lambda x: (x + 255) // 256 * 256
-    assert sa.attn_bwd_workspace_size(1, 1, 100, 64) == a256(100 * 4) + a256(100 * 64 * 4)
-    assert sa.attn_bwd_workspace_size(2, 16, 16384, 128) == a256(2 * 16 * 16384 * 4) + a256(2 * 16 * 16384 * 128 * 4)
+    assert sa.attn_bwd_workspace_size(1, 1, 100, 64) == 2 * a256(128 * 4) + a256(100 * 64 * 4)
+    assert (sa.attn_bwd_workspace_size(2, 16, 16384, 128)
+            == 2 * a256(32 * 16384 * 4) + a256(32 * 16384 * 128 * 4))
     assert sa.attn_bwd_workspace_size(1, 1, 100, 96) == 0
     assert sa.attn_bwd_workspace_size(0, 1, 100, 64) == 0
 
@@ -97,9 +98,10 @@ def test_bwd_argument_errors(lib):
     assert bwd(dq=dk) == 1
     assert bwd(dq=dq + 2) == 3
     assert bwd(o=0) == 1
-    assert lib.attn_bwd_main(Q, K, V, 0x60000000, L, dk, dv, ws, need - 16, 1, 2, 64, 64,
+    assert lib.attn_bwd_main(Q, K, V, 0x60000000, dk, dv, ws, need - 16, 1, 2, 64, 64,
                              ctypes.c_float(0.125), None) == 6
-    assert lib.attn_bwd_preprocess(O, 0, ws, need, 1, 2, 64, 64, None) == 1
+    assert lib.attn_bwd_preprocess(O, 0, L, ws, need, 1, 2, 64, 64, None) == 1
+    assert lib.attn_bwd_preprocess(O, 0x60000000, 0, ws, need, 1, 2, 64, 64, None) == 1
     assert lib.attn_bwd_dq_convert(ws, need, 0, 1, 2, 64, 64, ctypes.c_float(0.125), None) == 1
 
 

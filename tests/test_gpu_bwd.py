@@ -172,3 +172,21 @@ def test_wait_timeout_reports_status():
     o, lse = sa.forward(inp["q"].cuda(), inp["k"].cuda(), inp["v"].cuda())
     torch.cuda.synchronize()
     assert sa.attn_get_device_status() == 0
+
+
+def test_bwd_phases_match_single_call():
+    """attn_bwd_preprocess + attn_bwd_main + attn_bwd_dq_convert == attn_bwd."""
+    inp = make_qkv(2, 2, 321, 128, seed=27)
+    q, k, v, do = (inp[x].cuda() for x in ("q", "k", "v", "do"))
+    B, H, N, D = q.shape
+    o, lse = sa.forward(q, k, v)
+    dq1, dk1, dv1 = sa.backward(q, k, v, o, do, lse)
+    nbytes = sa.attn_bwd_workspace_size(B, H, N, D)
+    ws = torch.full((nbytes,), 0xAB, dtype=torch.uint8, device="cuda")   # garbage on entry
+    dq2, dk2, dv2 = (torch.empty_like(q) for _ in range(3))
+    sa.attn_bwd_preprocess(o, do, lse, ws, nbytes, B, H, N, D)
+    sa.attn_bwd_main(q, k, v, do, dk2, dv2, ws, nbytes, B, H, N, D, 1 / math.sqrt(D))
+    sa.attn_bwd_dq_convert(ws, nbytes, dq2, B, H, N, D, 1 / math.sqrt(D))
+    assert sa.attn_get_device_status() == 0
+    assert torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
+    check_grad("dq", dq2.float().cpu().numpy(), dq1.double().cpu().numpy(), "phases")
