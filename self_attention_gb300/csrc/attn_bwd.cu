@@ -38,15 +38,15 @@ template <int D>
 struct BwdCfg {
     static constexpr int BN = 128;   // keys per CTA (TMEM lanes of S^T, dP^T, dK, dV)
     static constexpr int BM = 64;    // queries per inner tile
-    static constexpr int QST = (D == 64) ? 4 : 2;  // (Q, dO, LSE2, D) ring depth
+    static constexpr int QST = (D == 64) ? 6 : 3;  // (Q, dO, LSE2, D) ring depth
     static constexpr int KV_BYTES = BN * D * 2;
     static constexpr int Q_BYTES = BM * D * 2;
-    // one ring stage: Q_i, dO_i (swizzled tiles), then LSE2_i and D_i (64 fp32 each), padded
-    // to keep every tile 1024-byte aligned
-    static constexpr int STAGE_BYTES = 2 * Q_BYTES + 1024;
+    static constexpr int STAGE_BYTES = 2 * Q_BYTES;   // Q_i then dO_i (swizzled tiles)
+    static constexpr int LD_BYTES = 2 * BM * 4;       // LSE2_i then D_i (fp32) per stage
     static constexpr int DS_BYTES = BN * BM * 2;
-    static constexpr int DQ_BYTES = BM * D * 4;
-    static constexpr int SMEM_BYTES = 2 * KV_BYTES + QST * STAGE_BYTES + 2 * DS_BYTES + DQ_BYTES + 1024;
+    static constexpr int DQH_BYTES = (BM / 2) * D * 4;  // dQ staging: half a query tile
+    static constexpr int SMEM_BYTES =
+        2 * KV_BYTES + QST * STAGE_BYTES + 2 * DS_BYTES + DQH_BYTES + QST * LD_BYTES + 1024;
     static constexpr int THREADS = 320;
     static constexpr uint32_t TM_DK = 0, TM_DV = D, TM_BUF = 2 * D;
     __host__ __device__ static constexpr uint32_t tm_s(int b) { return TM_BUF + b * 128; }
@@ -137,9 +137,10 @@ __global__ void __launch_bounds__(320, 1)
     uint8_t *smem = align1024(smem_raw);
     uint8_t *sK = smem;
     uint8_t *sV = sK + C::KV_BYTES;
-    uint8_t *sQ = sV + C::KV_BYTES;                 // QST stages of {Q_i, dO_i, LSE2_i, D_i}
+    uint8_t *sQ = sV + C::KV_BYTES;                 // QST stages of {Q_i, dO_i}
     uint8_t *sDS = sQ + C::QST * C::STAGE_BYTES;    // two dS^T tiles
-    float *sDQ = reinterpret_cast<float *>(sDS + 2 * C::DS_BYTES);  // dQ_i staging [BM][D]
+    float *sDQ = reinterpret_cast<float *>(sDS + 2 * C::DS_BYTES);  // dQ staging [BM/2][D]
+    float *sLD = reinterpret_cast<float *>(sDS + 2 * C::DS_BYTES + C::DQH_BYTES);  // QST x {LSE2, D}
 
     __shared__ uint64_t bar_kv, bar_qf[C::QST], bar_qe[C::QST];
     __shared__ uint64_t bar_sdp[2], bar_ds_full[2], bar_ds_empty[2], bar_dq_full[2], bar_dq_empty[2];
@@ -196,7 +197,7 @@ __global__ void __launch_bounds__(320, 1)
                 const int s = it % C::QST;
                 const uint32_t ph = (it / C::QST) & 1;
                 wait_bounded(&bar_qe[s], ph ^ 1, g);
-                ptx::mbar_arrive_expect_tx(&bar_qf[s], 2 * C::Q_BYTES + 2 * C::BM * 4);
+                ptx::mbar_arrive_expect_tx(&bar_qf[s], C::STAGE_BYTES + C::LD_BYTES);
                 uint8_t *stage = sQ + s * C::STAGE_BYTES;
                 for (int h = 0; h < D / 64; ++h) {
                     ptx::tma_load_3d(stage + h * C::BM * 128, &tm_q, &bar_qf[s], h * 64, it * C::BM, bh);
@@ -204,8 +205,8 @@ __global__ void __launch_bounds__(320, 1)
                                      h * 64, it * C::BM, bh);
                 }
                 const size_t rowvec = (size_t)bh * n_pad + (size_t)it * C::BM;
-                ptx::bulk_load(stage + 2 * C::Q_BYTES, lse2 + rowvec, C::BM * 4, &bar_qf[s]);
-                ptx::bulk_load(stage + 2 * C::Q_BYTES + C::BM * 4, dvec + rowvec, C::BM * 4, &bar_qf[s]);
+                ptx::bulk_load(sLD + s * 2 * C::BM, lse2 + rowvec, C::BM * 4, &bar_qf[s]);
+                ptx::bulk_load(sLD + s * 2 * C::BM + C::BM, dvec + rowvec, C::BM * 4, &bar_qf[s]);
             }
             wait_bounded(&bar_kv, 0, g);
             for (int it = (nq > C::QST ? nq - C::QST : 0); it < nq; ++it)
@@ -295,7 +296,7 @@ __global__ void __launch_bounds__(320, 1)
             const int b = it & 1, s = it % C::QST;
             const uint32_t ph = (it >> 1) & 1;
             // this query tile's LSE2 (+inf past N) and D (0 past N), loaded with the tile
-            const float *sl = reinterpret_cast<const float *>(sQ + s * C::STAGE_BYTES + 2 * C::Q_BYTES);
+            const float *sl = sLD + s * 2 * C::BM;
             const float *sd = sl + C::BM;
             wait_bounded(&bar_sdp[b], ph, g);
             wait_bounded(&bar_ds_empty[b], ph ^ 1, g);
@@ -383,22 +384,27 @@ __global__ void __launch_bounds__(320, 1)
             }
             ptx::tc_fence_before();
             ptx::mbar_arrive(&bar_dq_empty[b]);
-            if (leader) ptx::bulk_wait_group_read<0>();   // staging buffer free again
-            ptx::named_bar(2, 128);
-            if (r < D) {
-                const uint32_t base = opaque(ptx::smem_u32(sDQ) + r * 4);
+            // two halves of 32 query rows through one 32 x D staging buffer
 #pragma unroll
-                for (int c = 0; c < 32; ++c) sts_f32(base + c * D * 4, __uint_as_float(v0[c]));
+            for (int half = 0; half < 2; ++half) {
+                if (leader) ptx::bulk_wait_group_read<0>();   // staging buffer free again
+                ptx::named_bar(2, 128);
+                if (r < D) {
+                    const uint32_t base = opaque(ptx::smem_u32(sDQ) + r * 4);
 #pragma unroll
-                for (int c = 0; c < 32; ++c) sts_f32(base + (32 + c) * D * 4, __uint_as_float(v1[c]));
-            }
-            ptx::fence_proxy_async_smem();
-            ptx::named_bar(2, 128);
-            if (leader) {
-                const int q0 = it * C::BM;
-                const int rows = (n - q0) < C::BM ? (n - q0) : C::BM;
-                ptx::bulk_reduce_add_f32(dq_acc + ((size_t)bh * n + q0) * D, sDQ, (uint32_t)rows * D * 4);
-                ptx::bulk_commit_group();
+                    for (int c = 0; c < 32; ++c)
+                        sts_f32(base + c * D * 4, __uint_as_float(half == 0 ? v0[c] : v1[c]));
+                }
+                ptx::fence_proxy_async_smem();
+                ptx::named_bar(2, 128);
+                if (leader) {
+                    const int q0 = it * C::BM + half * 32;
+                    const int rows = (n - q0) < 32 ? (n - q0) : 32;
+                    if (rows > 0) {
+                        ptx::bulk_reduce_add_f32(dq_acc + ((size_t)bh * n + q0) * D, sDQ, (uint32_t)rows * D * 4);
+                        ptx::bulk_commit_group();
+                    }
+                }
             }
         }
         if (leader) ptx::bulk_wait_group<0>();
