@@ -48,7 +48,8 @@ typedef enum {
     ATTN_ERR_LAUNCH = 4,          /* the CUDA runtime refused a launch or a query */
     ATTN_ERR_TIMEOUT = 5,         /* a kernel wait gave up (reported by attn_get_device_status) */
     ATTN_ERR_WORKSPACE = 6,       /* workspace null, misaligned or smaller than required */
-    ATTN_ERR_DEVICE = 7           /* the current device is not an sm_103 GPU */
+    ATTN_ERR_DEVICE = 7,          /* the current device is not an sm_103 GPU */
+    ATTN_ERR_TOO_LARGE = 8        /* attn_bwd_noalloc: sizes need more than its fixed scratch */
 } attn_status;
 
 /*
@@ -134,6 +135,29 @@ const char *attn_last_error_string(void);
  * Used to test the failure path without hanging or faulting the GPU.
  */
 attn_status attn_debug_wait_timeout(unsigned limit_us, cudaStream_t stream);
+
+/*
+ * attn_bwd_noalloc: the backward pass without any workspace argument, for callers that cannot
+ * allocate device memory at the point where they run the backward: code that must not call
+ * cudaMalloc (or an allocator built on it) there, for example because it runs under a memory
+ * budget fixed up front or inside a framework that owns all device allocations.  The article
+ * has no counterpart; this is a convenience of this library.
+ *
+ * Arguments and results are those of attn_bwd() without `workspace` / `workspace_bytes`.  The
+ * scratch attn_bwd keeps in the workspace (attn_bwd_workspace_size(B,H,N,d_k) bytes) comes
+ * instead from one array of 64 MiB compiled into the library; every GPU that loads the library
+ * holds it until the process exits.  Sizes whose scratch exceeds 64 MiB are refused with
+ * ATTN_ERR_TOO_LARGE before anything is launched.  The call allocates no device memory.
+ *
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress) and
+ * caches it; make that first call before any stream capture.  All calls share the one array:
+ * calls whose work can overlap on the GPU (different streams, or different host threads without
+ * ordering) race on it and produce wrong gradients; order them on one stream.  Each call
+ * rewrites everything it reads from the array, so earlier contents do not matter.
+ */
+attn_status attn_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
+                             const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                             int B, int H, int N, int d_k, float scale, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -25,18 +25,19 @@ from .build import LIB_PATH
 __all__ = [
     "AttnError", "attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess",
     "attn_bwd_main", "attn_bwd_dq_convert", "attn_get_device_status",
-    "attn_status_string", "attn_last_error_string", "attn_debug_wait_timeout", "forward", "backward", "attention",
+    "attn_status_string", "attn_last_error_string", "attn_debug_wait_timeout", "attn_bwd_noalloc",
+    "forward", "backward", "attention",
     "load_library", "STATUS",
 ]
 
 STATUS = {
     0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED_DK",
     3: "ATTN_ERR_MISALIGNED", 4: "ATTN_ERR_LAUNCH", 5: "ATTN_ERR_TIMEOUT",
-    6: "ATTN_ERR_WORKSPACE", 7: "ATTN_ERR_DEVICE",
+    6: "ATTN_ERR_WORKSPACE", 7: "ATTN_ERR_DEVICE", 8: "ATTN_ERR_TOO_LARGE",
 }
 EXPORTS = ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess",
            "attn_bwd_main", "attn_bwd_dq_convert", "attn_get_device_status", "attn_status_string",
-           "attn_last_error_string", "attn_debug_wait_timeout")
+           "attn_last_error_string", "attn_debug_wait_timeout", "attn_bwd_noalloc")
 
 
 class AttnError(RuntimeError):
@@ -80,6 +81,8 @@ def load_library(path: str = LIB_PATH):
     lib.attn_status_string.restype = ctypes.c_char_p
     lib.attn_last_error_string.argtypes = []
     lib.attn_last_error_string.restype = ctypes.c_char_p
+    lib.attn_bwd_noalloc.argtypes = [_VP] * 9 + [_I] * 4 + [_F, _VP]
+    lib.attn_bwd_noalloc.restype = _I
     lib.attn_debug_wait_timeout.argtypes = [ctypes.c_uint, _VP]
     lib.attn_debug_wait_timeout.restype = _I
     if path == LIB_PATH:
@@ -154,6 +157,16 @@ def attn_bwd_dq_convert(workspace, workspace_bytes: int, dq, B: int, H: int, N: 
     _raise(load_library().attn_bwd_dq_convert(_ptr(workspace), int(workspace_bytes), _ptr(dq), B,
                                               H, N, d_k, float(scale), _stream(stream)),
            "attn_bwd_dq_convert")
+
+
+def attn_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B: int, H: int, N: int, d_k: int,
+                     scale: float, stream=None):
+    """attn_bwd without a workspace: for callers that cannot allocate device memory.  The
+    scratch is a fixed 64 MiB array inside the library, shared by every call (order calls on
+    one stream; overlapping calls race)."""
+    _raise(load_library().attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout),
+                                           _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d_k,
+                                           float(scale), _stream(stream)), "attn_bwd_noalloc")
 
 
 def attn_get_device_status(stream=None) -> int:

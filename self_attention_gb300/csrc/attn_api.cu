@@ -351,6 +351,8 @@ extern "C" const char *attn_status_string(attn_status status)
     case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT: a kernel wait gave up";
     case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE: workspace missing, misaligned or too small";
     case ATTN_ERR_DEVICE: return "ATTN_ERR_DEVICE: the current device is not an sm_103 GPU";
+    case ATTN_ERR_TOO_LARGE:
+        return "ATTN_ERR_TOO_LARGE: the sizes need more scratch than attn_bwd_noalloc's fixed 64 MiB";
     }
     return "unknown attn_status";
 }
@@ -389,3 +391,64 @@ cudaError_t launch_wait_selftest(int *status, uint64_t limit_ns, cudaStream_t st
     return cudaGetLastError();
 }
 }  // namespace attn
+
+// --------------------------------------------------------------------------------------------
+// attn_bwd_noalloc: attn_bwd for callers that cannot allocate device memory.  Its scratch (the
+// D and LSE2 vectors and the fp32 dQ accumulator that attn_bwd keeps in the caller's
+// workspace) lives in one fixed array compiled into the library.
+namespace attn {
+
+constexpr size_t kNoAllocScratchBytes = 64ull << 20;
+
+// Every GPU that loads this library holds this array (64 MiB) until the process exits.  In host
+// code its name is only a stand-in for the symbol, never a device address: the address comes
+// from cudaGetSymbolAddress, once per device, below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+std::mutex g_scratch_mutex;
+void *g_scratch_addr[kMaxDevices];  // device address of g_noalloc_scratch, per device
+}  // namespace
+}  // namespace attn
+
+extern "C" attn_status attn_bwd_noalloc(const void *q, const void *k, const void *v,
+                                        const void *o, const void *dout, const float *lse,
+                                        void *dq, void *dk, void *dv, int B, int H, int N,
+                                        int d_k, float scale, cudaStream_t stream)
+{
+    attn_status st = check_sizes(B, H, N, d_k, scale);
+    if (st != ATTN_OK) return st;
+    const size_t need = attn_bwd_workspace_size(B, H, N, d_k);
+    if (need > kNoAllocScratchBytes) return ATTN_ERR_TOO_LARGE;
+
+    // device_state() makes this thread's current device current in the driver too, which
+    // cudaGetSymbolAddress needs; the address is looked up once per device and cached.
+    DeviceState *dev = nullptr;
+    if ((st = device_state(&dev)) != ATTN_OK) return st;
+    int id = 0;
+    cudaError_t e = cudaGetDevice(&id);
+    if (e != cudaSuccess) return fail("cudaGetDevice", e);
+    void *scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_scratch_mutex);
+        if (!g_scratch_addr[id]) {
+            void *p = nullptr;
+            e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+            if (e != cudaSuccess || !p) return fail("cudaGetSymbolAddress(g_noalloc_scratch)", e);
+            g_scratch_addr[id] = p;
+        }
+        scratch = g_scratch_addr[id];
+    }
+
+    // The same three phases as attn_bwd; the preprocess phase rewrites every scratch byte the
+    // later phases read (D, LSE2 and the zeroed accumulator), so what an earlier call left in
+    // the array does not matter.
+    BwdArgs a;
+    st = prepare_bwd(a, kPre | kMain | kConv, q, k, v, o, dout, lse, dq, dk, dv, scratch,
+                     kNoAllocScratchBytes, B, H, N, d_k, scale);
+    if (st != ATTN_OK) return st;
+    e = launch_bwd_preprocess(a, stream);
+    if (e == cudaSuccess) e = launch_bwd_main(a, stream);
+    if (e == cudaSuccess) e = launch_bwd_convert(a, stream);
+    return e == cudaSuccess ? ATTN_OK : fail("attn_bwd_noalloc launch", e);
+}
