@@ -13,18 +13,21 @@
 //      of 64 with D = 0, LSE2 = +inf so that padded queries get zero probability), and zero
 //      the fp32 dQ accumulator.
 //   2. main: one CTA per 128-key tile j of one head, looping over all 64-row query tiles i.
-//        warp 8     TMA producer: K_j and V_j once; a ring of (Q_i, dO_i, LSE2_i, D_i).
-//        warp 9     tcgen05 issuer, per query tile:
-//                     S^T = K_j Q_i^T, dP^T = V_j dO_i^T          (into TMEM, double-buffered)
-//                     dV += P^T dO_i  (P^T from TMEM), dK += dS^T Q_i, dQ_i^T = K_j^T dS^T
-//        warps 0-3  thread = key row: P^T = 2^(S^T c - LSE log2 e), dS^T = P^T o (dP^T - D);
-//                   P^T (bf16) goes back into TMEM over S^T, dS^T (bf16) into shared memory.
-//                   At the end they write dK (times scale) and dV in bf16.
-//        warps 4-7  thread = one of the d columns: move dQ_i^T from TMEM to shared memory
-//                   (transposed to dQ_i rows) and add it into the fp32 accumulator with one
-//                   bulk reduce-add per tile (fp32 atomics in L2: low bits vary run to run).
+//        warp 12     TMA producer: K_j and V_j once; a ring of (Q_i, dO_i, LSE2_i, D_i).
+//        warp 13     tcgen05 issuer, per query tile i (TMEM buffer b = i & 1):
+//                      dV += P^T dO_i (P^T from TMEM), dQ_i^T = K_j^T dS^T (over P^T),
+//                      dK += dS^T Q_i, then dP^T = V_j dO^T and S^T = K_j Q^T of tile i + 2.
+//        warps 0-7   two warpgroups, alternating query tiles; thread = key row:
+//                    P^T = 2^(S^T c - LSE log2 e), dS^T = P^T o (dP^T - D); P^T (bf16) goes back
+//                    into TMEM over S^T, dS^T (bf16) into shared memory.  At the end group 0
+//                    writes dK (times scale) and group 1 writes dV, in bf16.
+//        warps 8-11  thread = one of the d columns: move dQ_i^T from TMEM to shared memory
+//                    (transposed to dQ_i rows, two double-buffered halves) and add it into the
+//                    fp32 accumulator with bulk reduce-adds (fp32 atomics in L2, whose
+//                    throughput, ~6 TB/s on this part, bounds this loop; low bits of dQ vary
+//                    from run to run).
 //   3. convert: dQ = bf16(scale * accumulator).
-// TMEM columns: dK [0,d), dV [d,2d), then two buffers of {S^T/P^T (64), dP^T/dQ^T (64)}.
+// TMEM columns: dK [0,d), dV [d,2d), then two buffers of {S^T/P^T/dQ^T (64), dP^T (64)}.
 // dQ^T has M = d rows; for d = 64 the MMA still runs with M = 128 and lanes 64-127 are unused.
 #include "common.cuh"
 #include "kernels.h"
@@ -46,8 +49,8 @@ struct BwdCfg {
     static constexpr int DS_BYTES = BN * BM * 2;
     static constexpr int DQH_BYTES = (BM / 2) * D * 4;  // dQ staging: half a query tile
     static constexpr int SMEM_BYTES =
-        2 * KV_BYTES + QST * STAGE_BYTES + 2 * DS_BYTES + DQH_BYTES + QST * LD_BYTES + 1024;
-    static constexpr int THREADS = 320;
+        2 * KV_BYTES + QST * STAGE_BYTES + 2 * DS_BYTES + 2 * DQH_BYTES + QST * LD_BYTES + 1024;
+    static constexpr int THREADS = 448;
     static constexpr uint32_t TM_DK = 0, TM_DV = D, TM_BUF = 2 * D;
     __host__ __device__ static constexpr uint32_t tm_s(int b) { return TM_BUF + b * 128; }
     __host__ __device__ static constexpr uint32_t tm_dp(int b) { return TM_BUF + b * 128 + 64; }
@@ -124,7 +127,7 @@ __global__ void __launch_bounds__(256)
 
 // ------------------------------------------------------------------ 2. main
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(448, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const float *__restrict__ lse2, const float *__restrict__ dvec,
@@ -139,8 +142,8 @@ __global__ void __launch_bounds__(320, 1)
     uint8_t *sV = sK + C::KV_BYTES;
     uint8_t *sQ = sV + C::KV_BYTES;                 // QST stages of {Q_i, dO_i}
     uint8_t *sDS = sQ + C::QST * C::STAGE_BYTES;    // two dS^T tiles
-    float *sDQ = reinterpret_cast<float *>(sDS + 2 * C::DS_BYTES);  // dQ staging [BM/2][D]
-    float *sLD = reinterpret_cast<float *>(sDS + 2 * C::DS_BYTES + C::DQH_BYTES);  // QST x {LSE2, D}
+    float *sDQ = reinterpret_cast<float *>(sDS + 2 * C::DS_BYTES);  // 2 x dQ staging [BM/2][D]
+    float *sLD = reinterpret_cast<float *>(sDS + 2 * C::DS_BYTES + 2 * C::DQH_BYTES);  // QST x {LSE2, D}
 
     __shared__ uint64_t bar_kv, bar_qf[C::QST], bar_qe[C::QST];
     __shared__ uint64_t bar_sdp[2], bar_ds_full[2], bar_ds_empty[2], bar_dq_full[2], bar_dq_empty[2];
@@ -172,7 +175,7 @@ __global__ void __launch_bounds__(320, 1)
         ptx::mbar_init(&bar_done, 1);
         ptx::fence_mbar_init();
     }
-    if (warp == 9) {
+    if (warp == 13) {
         ptx::tmem_alloc(&tmem_sh, 512);
         ptx::tmem_relinquish();
     }
@@ -181,7 +184,7 @@ __global__ void __launch_bounds__(320, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = tmem_sh;
 
-    if (warp == 8) {
+    if (warp == 12) {
         // ---------------------------------------------------------------- TMA producer
         if (ptx::elect_one()) {
             ptx::tma_prefetch_desc(&tm_q);
@@ -212,7 +215,7 @@ __global__ void __launch_bounds__(320, 1)
             for (int it = (nq > C::QST ? nq - C::QST : 0); it < nq; ++it)
                 wait_bounded(&bar_qf[it % C::QST], (it / C::QST) & 1, g);
         }
-    } else if (warp == 9) {
+    } else if (warp == 13) {
         // ---------------------------------------------------------------- MMA issuer
         if (ptx::elect_one()) {
             const uint32_t idSdP = ptx::idesc_bf16_f32(128, C::BM, false, false);
@@ -223,7 +226,7 @@ __global__ void __launch_bounds__(320, 1)
             auto qs = [&](int s) { return q_base + s * C::STAGE_BYTES; };
             auto dos = [&](int s) { return q_base + s * C::STAGE_BYTES + C::Q_BYTES; };
             // S^T = K_j Q_i^T and dP^T = V_j dO_i^T: all four operands K-major over d.
-            auto issue_sdp = [&](int s, int b) {
+            auto issue_s = [&](int s, int b) {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t offa = (kk >> 2) * (C::BN * 128) + (kk & 3) * 32;
@@ -231,6 +234,8 @@ __global__ void __launch_bounds__(320, 1)
                     ptx::mma_ss(tmem + C::tm_s(b), ptx::sdesc_sw128(k_base + offa, 16, 1024),
                                 ptx::sdesc_sw128(qs(s) + offb, 16, 1024), idSdP, kk > 0 ? 1u : 0u);
                 }
+            };
+            auto issue_dp = [&](int s, int b) {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t offa = (kk >> 2) * (C::BN * 128) + (kk & 3) * 32;
@@ -239,61 +244,80 @@ __global__ void __launch_bounds__(320, 1)
                                 ptx::sdesc_sw128(dos(s) + offb, 16, 1024), idSdP, kk > 0 ? 1u : 0u);
                 }
             };
-            auto issue_grads = [&](int s, int b, bool acc) {
-                // dV += P^T dO_i: A = P^T (TMEM, 8 columns per 16 queries), B = dO_i MN-major.
+            // dV += P^T dO_i: A = P^T (TMEM, 8 columns per 16 queries), B = dO_i MN-major.
+            auto issue_dv = [&](int s, int b, bool acc) {
 #pragma unroll
                 for (int kk = 0; kk < C::BM / 16; ++kk)
                     ptx::mma_ts(tmem + C::TM_DV, tmem + C::tm_s(b) + kk * 8,
                                 ptx::sdesc_sw128(dos(s) + kk * 2048, C::BM * 128, 1024), idKV,
                                 (acc || kk > 0) ? 1u : 0u);
-                // dK += dS^T Q_i: A = dS^T K-major (queries contiguous), B = Q_i MN-major.
+            };
+            // dK += dS^T Q_i: A = dS^T K-major (queries contiguous), B = Q_i MN-major.
+            auto issue_dk = [&](int s, int b, bool acc) {
 #pragma unroll
                 for (int kk = 0; kk < C::BM / 16; ++kk)
                     ptx::mma_ss(tmem + C::TM_DK, ptx::sdesc_sw128(ds_base + b * C::DS_BYTES + kk * 32, 16, 1024),
                                 ptx::sdesc_sw128(qs(s) + kk * 2048, C::BM * 128, 1024), idKV,
                                 (acc || kk > 0) ? 1u : 0u);
-                // dQ_i^T = K_j^T dS^T: A = K_j MN-major (M = d; halves BN*128 bytes apart),
-                // B = dS^T MN-major (N = 64 queries), K = 128 keys.
+            };
+            // dQ_i^T = K_j^T dS^T into the S^T / P^T columns (free once dV has read P^T):
+            // A = K_j MN-major (M = d; halves BN*128 bytes apart), B = dS^T MN-major (N = 64
+            // queries), K = 128 keys.
+            auto issue_dq = [&](int b) {
 #pragma unroll
                 for (int kk = 0; kk < C::BN / 16; ++kk)
-                    ptx::mma_ss(tmem + C::tm_dp(b), ptx::sdesc_sw128(k_base + kk * 2048, C::BN * 128, 1024),
+                    ptx::mma_ss(tmem + C::tm_s(b), ptx::sdesc_sw128(k_base + kk * 2048, C::BN * 128, 1024),
                                 ptx::sdesc_sw128(ds_base + b * C::DS_BYTES + kk * 2048, C::BN * 128, 1024),
                                 idDQ, kk > 0 ? 1u : 0u);
             };
+            // Per query tile i (buffer b = i & 1): dV, dQ_i^T (over P^T), dK, then tile i + 2's
+            // dP^T (its columns are free) and, once the dQ warps have drained dQ_i^T, its S^T.
+            // The drain overlaps dK and dP^T; tile i + 1's products, issued one step earlier,
+            // keep the other P / dS warpgroup busy meanwhile.
             wait_bounded(&bar_kv, 0, g);
-            wait_bounded(&bar_qf[0], 0, g);
-            ptx::tc_fence_after();
-            issue_sdp(0, 0);
-            ptx::mma_commit(&bar_sdp[0]);
+            for (int j = 0; j < 2 && j < nq; ++j) {
+                wait_bounded(&bar_qf[j % C::QST], (j / C::QST) & 1, g);
+                ptx::tc_fence_after();
+                issue_s(j % C::QST, j);
+                issue_dp(j % C::QST, j);
+                ptx::mma_commit(&bar_sdp[j]);
+            }
             for (int it = 0; it < nq; ++it) {
                 const int b = it & 1, s = it % C::QST;
-                if (it + 1 < nq) {
-                    const int s1 = (it + 1) % C::QST, b1 = b ^ 1;
-                    wait_bounded(&bar_qf[s1], ((it + 1) / C::QST) & 1, g);
-                    wait_bounded(&bar_dq_empty[b1], (((it + 1) >> 1) & 1) ^ 1, g);
-                    ptx::tc_fence_after();
-                    issue_sdp(s1, b1);
-                    ptx::mma_commit(&bar_sdp[b1]);
-                }
                 wait_bounded(&bar_ds_full[b], (it >> 1) & 1, g);
                 ptx::tc_fence_after();
-                issue_grads(s, b, it > 0);
+                issue_dv(s, b, it > 0);
+                issue_dq(b);
                 ptx::mma_commit(&bar_dq_full[b]);
+                issue_dk(s, b, it > 0);
                 ptx::mma_commit(&bar_qe[s]);
                 ptx::mma_commit(&bar_ds_empty[b]);
+                if (it + 2 < nq) {
+                    const int s2 = (it + 2) % C::QST;
+                    wait_bounded(&bar_qf[s2], ((it + 2) / C::QST) & 1, g);
+                    ptx::tc_fence_after();
+                    issue_dp(s2, b);
+                    wait_bounded(&bar_dq_empty[b], (it >> 1) & 1, g);   // dQ_i^T drained
+                    ptx::tc_fence_after();
+                    issue_s(s2, b);
+                    ptx::mma_commit(&bar_sdp[b]);
+                }
             }
             ptx::mma_commit(&bar_dkv);
             ptx::mma_commit(&bar_done);
             wait_bounded(&bar_done, 0, g);
         }
-    } else if (warp < 4) {
-        // ---------------------------------------------------------------- P / dS warpgroup
-        const int r = warp * 32 + lane;     // key row within the tile = TMEM lane
+    } else if (warp < 8) {
+        // ---------------------------------------------------------------- P / dS warpgroups
+        // Warpgroup wg takes the query tiles i = wg, wg + 2, ... (TMEM buffer b = wg), so the
+        // two groups overlap their element-wise work.
+        const int wg = warp >> 2, cw = warp & 3;
+        const int r = cw * 32 + lane;       // key row within the tile = TMEM lane
         const bool key_ok = kv0 + r < n;
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const uint32_t lane_off = (uint32_t)(cw * 32) << 16;
         const float scale_log2 = scale * kLog2e;
-        for (int it = 0; it < nq; ++it) {
-            const int b = it & 1, s = it % C::QST;
+        for (int it = wg; it < nq; it += 2) {
+            const int b = wg, s = it % C::QST;
             const uint32_t ph = (it >> 1) & 1;
             // this query tile's LSE2 (+inf past N) and D (0 past N), loaded with the tile
             const float *sl = sLD + s * 2 * C::BM;
@@ -302,36 +326,50 @@ __global__ void __launch_bounds__(320, 1)
             wait_bounded(&bar_ds_empty[b], ph ^ 1, g);
             ptx::tc_fence_after();
             uint8_t *rowp = sDS + b * C::DS_BYTES + r * 128;
+            const uint32_t tS = tmem + lane_off + C::tm_s(b), tDP = tmem + lane_off + C::tm_dp(b);
+            // 16 queries at a time; the next quarter's TMEM loads overlap this quarter's math.
+            // P^T of quarter q goes to columns [8q, 8q + 8), over S^T columns already read.
+            uint32_t sv[2][16], dpv[2][16];
+            ptx::tmem_ld16(tS, sv[0]);
+            ptx::tmem_ld16(tDP, dpv[0]);
+            ptx::tmem_ld_wait();
+            reg_fence(sv[0]);
+            reg_fence(dpv[0]);
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t sv[32], dpv[32], pp[16], dsp[16];
-                ptx::tmem_ld32(tmem + lane_off + C::tm_s(b) + half * 32, sv);
-                ptx::tmem_ld32(tmem + lane_off + C::tm_dp(b) + half * 32, dpv);
-                ptx::tmem_ld_wait();
-                reg_fence(sv);
-                reg_fence(dpv);
+            for (int qt = 0; qt < 4; ++qt) {
+                const int cur = qt & 1;
+                if (qt < 3) {
+                    ptx::tmem_ld16(tS + (qt + 1) * 16, sv[cur ^ 1]);
+                    ptx::tmem_ld16(tDP + (qt + 1) * 16, dpv[cur ^ 1]);
+                }
+                uint32_t pp[8], dsp[8];
 #pragma unroll
-                for (int c = 0; c < 32; c += 4) {
-                    const float4 l4 = *reinterpret_cast<const float4 *>(sl + half * 32 + c);
-                    const float4 d4 = *reinterpret_cast<const float4 *>(sd + half * 32 + c);
+                for (int c = 0; c < 16; c += 4) {
+                    const float4 l4 = *reinterpret_cast<const float4 *>(sl + qt * 16 + c);
+                    const float4 d4 = *reinterpret_cast<const float4 *>(sd + qt * 16 + c);
                     const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
                     float p[4], ds[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        p[e] = ptx::ex2(fmaf(__uint_as_float(sv[c + e]), scale_log2, -lv[e]));
+                        p[e] = ptx::ex2(fmaf(__uint_as_float(sv[cur][c + e]), scale_log2, -lv[e]));
                         if (!key_ok) p[e] = 0.f;
-                        ds[e] = p[e] * (__uint_as_float(dpv[c + e]) - dv4[e]);
+                        ds[e] = p[e] * (__uint_as_float(dpv[cur][c + e]) - dv4[e]);
                     }
                     pp[c / 2] = ptx::pack_bf16x2(p[0], p[1]);
                     pp[c / 2 + 1] = ptx::pack_bf16x2(p[2], p[3]);
                     dsp[c / 2] = ptx::pack_bf16x2(ds[0], ds[1]);
                     dsp[c / 2 + 1] = ptx::pack_bf16x2(ds[2], ds[3]);
                 }
-                ptx::tmem_st16(tmem + lane_off + C::tm_s(b) + half * 16, pp);
+                ptx::tmem_st8(tS + qt * 8, pp);
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
-                    *reinterpret_cast<uint4 *>(rowp + (((half * 4 + cc) ^ (r & 7)) << 4)) =
+                for (int cc = 0; cc < 2; ++cc)
+                    *reinterpret_cast<uint4 *>(rowp + (((qt * 2 + cc) ^ (r & 7)) << 4)) =
                         make_uint4(dsp[4 * cc], dsp[4 * cc + 1], dsp[4 * cc + 2], dsp[4 * cc + 3]);
+                if (qt < 3) {
+                    ptx::tmem_ld_wait();
+                    reg_fence(sv[cur ^ 1]);
+                    reg_fence(dpv[cur ^ 1]);
+                }
             }
             ptx::tmem_st_wait();
             ptx::fence_proxy_async_smem();
@@ -342,8 +380,8 @@ __global__ void __launch_bounds__(320, 1)
         wait_bounded(&bar_dkv, 0, g);
         ptx::tc_fence_after();
         const size_t row_off = ((size_t)bh * n + (key_ok ? kv0 + r : 0)) * D;
-#pragma unroll
-        for (int which = 0; which < 2; ++which) {
+        {   // warpgroup 0 writes dK (times scale), warpgroup 1 writes dV
+            const int which = wg;
             const float mul = which == 0 ? scale : 1.f;
             __nv_bfloat16 *dst_row = (which == 0 ? dk : dv) + row_off;
             const uint32_t col0 = which == 0 ? C::TM_DK : C::TM_DV;
@@ -367,30 +405,32 @@ __global__ void __launch_bounds__(320, 1)
         }
     } else {
         // ---------------------------------------------------------------- dQ warpgroup
-        const int r = (warp - 4) * 32 + lane;   // d column = TMEM lane of dQ^T
-        const uint32_t lane_off = (uint32_t)((warp - 4) * 32) << 16;
-        const bool leader = threadIdx.x == 128;
+        const int r = (warp - 8) * 32 + lane;   // d column = TMEM lane of dQ^T
+        const uint32_t lane_off = (uint32_t)((warp - 8) * 32) << 16;
+        const bool leader = threadIdx.x == 256;
         for (int it = 0; it < nq; ++it) {
             const int b = it & 1;
             wait_bounded(&bar_dq_full[b], (it >> 1) & 1, g);
             ptx::tc_fence_after();
             uint32_t v0[32], v1[32];
-            if ((warp - 4) * 32 < D) {
-                ptx::tmem_ld32(tmem + lane_off + C::tm_dp(b), v0);
-                ptx::tmem_ld32(tmem + lane_off + C::tm_dp(b) + 32, v1);
+            if ((warp - 8) * 32 < D) {
+                ptx::tmem_ld32(tmem + lane_off + C::tm_s(b), v0);
+                ptx::tmem_ld32(tmem + lane_off + C::tm_s(b) + 32, v1);
                 ptx::tmem_ld_wait();
                 reg_fence(v0);
                 reg_fence(v1);
             }
             ptx::tc_fence_before();
             ptx::mbar_arrive(&bar_dq_empty[b]);
-            // two halves of 32 query rows through one 32 x D staging buffer
+            // two halves of 32 query rows, each through its own 32 x D staging buffer, so that
+            // filling one overlaps the bulk reduce-add still reading the other
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-                if (leader) ptx::bulk_wait_group_read<0>();   // staging buffer free again
+                float *stage = sDQ + half * (C::DQH_BYTES / 4);
+                if (leader) ptx::bulk_wait_group_read<1>();   // this buffer's last reduce has read it
                 ptx::named_bar(2, 128);
                 if (r < D) {
-                    const uint32_t base = opaque(ptx::smem_u32(sDQ) + r * 4);
+                    const uint32_t base = opaque(ptx::smem_u32(stage) + r * 4);
 #pragma unroll
                     for (int c = 0; c < 32; ++c)
                         sts_f32(base + c * D * 4, __uint_as_float(half == 0 ? v0[c] : v1[c]));
@@ -401,7 +441,7 @@ __global__ void __launch_bounds__(320, 1)
                     const int q0 = it * C::BM + half * 32;
                     const int rows = (n - q0) < 32 ? (n - q0) : 32;
                     if (rows > 0) {
-                        ptx::bulk_reduce_add_f32(dq_acc + ((size_t)bh * n + q0) * D, sDQ, (uint32_t)rows * D * 4);
+                        ptx::bulk_reduce_add_f32(dq_acc + ((size_t)bh * n + q0) * D, stage, (uint32_t)rows * D * 4);
                         ptx::bulk_commit_group();
                     }
                 }
@@ -412,7 +452,7 @@ __global__ void __launch_bounds__(320, 1)
 
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == 13) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, 512);
     }
