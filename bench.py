@@ -325,6 +325,21 @@ def run_ours(args, world, rank, local):
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in out_host.values())
 
+    # HBM probe: section 2's vector add over three 512 MiB arrays (12 bytes per element moved)
+    nvec = 1 << 27
+    va, vb = torch.ones(nvec, device="cuda"), torch.ones(nvec, device="cuda")
+    vc = torch.empty_like(va)
+    sa.vector_add(va, vb, vc, nvec, stream)
+    torch.cuda.synchronize()
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    p0.record(stream)
+    for _ in range(10):
+        sa.vector_add(va, vb, vc, nvec, stream)
+    p1.record(stream)
+    torch.cuda.synchronize()
+    probe_gbs = 12.0 * nvec / (p0.elapsed_time(p1) / 10 * 1e-3) / 1e9
+    del va, vb, vc
+
     res = reduce_over_ranks(local_res, world)
     if rank != 0:
         dist.destroy_process_group()
@@ -365,6 +380,8 @@ def run_ours(args, world, rank, local):
                      "note": f"peak = {peak_src} sustained dense bf16; achieved = 10*B*H*N^2*d "
                              "flops per launch / CUDA-event launch time"},
         "cpu_baseline": cpu,
+        "hbm_probe": {"kernel": "vector_add (fp32, 3 x 512 MiB)", "gbs": probe_gbs,
+                      "frac_of_measured_copy": probe_gbs / peaks["hbm_gbs"]},
         "e2e": {"value": flops_total / (res["e2e_ms"] * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 4 * args.steps,

@@ -137,6 +137,17 @@ const char *attn_last_error_string(void);
 attn_status attn_debug_wait_timeout(unsigned limit_us, cudaStream_t stream);
 
 /*
+ * Element-wise fp32 addition c[i] = a[i] + b[i], 0 <= i < n: the vector_add_cuda kernel of
+ * section 2 ("Practical code comparison: raw CUDA C++ vs OpenAI Triton", the raw CUDA C++
+ * version: one element per index, guarded by i < n), used here as the library's HBM bandwidth
+ * probe (16-byte vector accesses, grid-stride over whole waves of the SMs).
+ *   a, b : n fp32 device inputs;  c : n fp32 device output (may be a or b itself; no other
+ *   overlap).  All 16-byte aligned.  n = 0 is a no-op; n < 0 is ATTN_ERR_INVALID_ARG.
+ * Each c[i] is the correctly rounded fp32 sum, bit for bit what one fp32 addition gives.
+ */
+attn_status vector_add(const float *a, const float *b, float *c, long long n, cudaStream_t stream);
+
+/*
  * attn_bwd_noalloc: the backward pass without any workspace argument, for callers that cannot
  * allocate device memory at the point where they run the backward: code that must not call
  * cudaMalloc (or an allocator built on it) there, for example because it runs under a memory

@@ -65,6 +65,9 @@ def load_library(path: str):
     for f in (lib.oracle_attn_fwd, lib.oracle_attn_bwd, lib.oracle_attn_fwd_rows,
               lib.oracle_attn_bwd_rows):
         f.restype = ctypes.c_int
+    _F = ctypes.POINTER(ctypes.c_float)
+    lib.oracle_vector_add.argtypes = [_F, _F, _F, i64]
+    lib.oracle_vector_add.restype = None
     return lib
 
 
@@ -158,3 +161,16 @@ def bwd_rows(q_head, k_head, v_head, do_head, qrows, krows, scale: float, lib=No
                                     qrows.size, krows.ctypes.data_as(_I64), krows.size, _p(dq),
                                     _p(dk), _p(dv), n, d, float(scale)))
     return dq, dk, dv
+
+
+def vector_add(a, b, lib=None):
+    """c = a + b element-wise in fp32 (section 2's vector add).  Returns a new float32 array."""
+    lib = lib or _get()
+    a = np.ascontiguousarray(a, dtype=np.float32).ravel()
+    b = np.ascontiguousarray(b, dtype=np.float32).ravel()
+    if a.size != b.size:
+        raise ValueError("a and b differ in length")
+    c = np.empty_like(a)
+    fp = ctypes.POINTER(ctypes.c_float)
+    lib.oracle_vector_add(a.ctypes.data_as(fp), b.ctypes.data_as(fp), c.ctypes.data_as(fp), a.size)
+    return c

@@ -286,3 +286,11 @@ int oracle_attn_bwd_rows(const double *q, const double *k, const double *v, cons
     free(dvec);
     return err;
 }
+
+/* Element-wise fp32 addition c = a + b ("Self-attention, CUDA kernels and FlashAttention",
+ * section 2: the vector_add_cuda kernel computes C[idx] = A[idx] + B[idx] for idx < N).  One
+ * fp32 addition per element, rounded to nearest even as IEEE 754 prescribes. */
+void oracle_vector_add(const float *a, const float *b, float *c, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) c[i] = a[i] + b[i];
+}

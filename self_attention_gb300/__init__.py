@@ -26,6 +26,7 @@ __all__ = [
     "AttnError", "attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess",
     "attn_bwd_main", "attn_bwd_dq_convert", "attn_get_device_status",
     "attn_status_string", "attn_last_error_string", "attn_debug_wait_timeout", "attn_bwd_noalloc",
+    "vector_add",
     "forward", "backward", "attention",
     "load_library", "STATUS",
 ]
@@ -37,7 +38,7 @@ STATUS = {
 }
 EXPORTS = ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess",
            "attn_bwd_main", "attn_bwd_dq_convert", "attn_get_device_status", "attn_status_string",
-           "attn_last_error_string", "attn_debug_wait_timeout", "attn_bwd_noalloc")
+           "attn_last_error_string", "attn_debug_wait_timeout", "attn_bwd_noalloc", "vector_add")
 
 
 class AttnError(RuntimeError):
@@ -81,6 +82,8 @@ def load_library(path: str = LIB_PATH):
     lib.attn_status_string.restype = ctypes.c_char_p
     lib.attn_last_error_string.argtypes = []
     lib.attn_last_error_string.restype = ctypes.c_char_p
+    lib.vector_add.argtypes = [_VP, _VP, _VP, ctypes.c_longlong, _VP]
+    lib.vector_add.restype = _I
     lib.attn_bwd_noalloc.argtypes = [_VP] * 9 + [_I] * 4 + [_F, _VP]
     lib.attn_bwd_noalloc.restype = _I
     lib.attn_debug_wait_timeout.argtypes = [ctypes.c_uint, _VP]
@@ -167,6 +170,12 @@ def attn_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B: int, H: int, N: int, 
     _raise(load_library().attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout),
                                            _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d_k,
                                            float(scale), _stream(stream)), "attn_bwd_noalloc")
+
+
+def vector_add(a, b, c, n: int, stream=None):
+    """c = a + b for n fp32 device elements (section 2's vector add; the HBM probe)."""
+    _raise(load_library().vector_add(_ptr(a), _ptr(b), _ptr(c), int(n), _stream(stream)),
+           "vector_add")
 
 
 def attn_get_device_status(stream=None) -> int:

@@ -369,6 +369,24 @@ extern "C" attn_status attn_debug_wait_timeout(unsigned limit_us, cudaStream_t s
 
 extern "C" const char *attn_last_error_string(void) { return t_last_error; }
 
+extern "C" attn_status vector_add(const float *a, const float *b, float *c, long long n,
+                                  cudaStream_t stream)
+{
+    if (n < 0) return ATTN_ERR_INVALID_ARG;
+    if (n == 0) return ATTN_OK;
+    if (!a || !b || !c) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned16(b) || !aligned16(c)) return ATTN_ERR_MISALIGNED;
+    const size_t bytes = (size_t)n * 4;
+    // c may be a or b (in-place addition is element-wise safe); partial overlaps are not
+    const Range rc = span(c, bytes), ra = span(a, bytes), rb = span(b, bytes);
+    if ((overlap(rc, ra) && c != a) || (overlap(rc, rb) && c != b)) return ATTN_ERR_INVALID_ARG;
+    DeviceState *dev = nullptr;
+    attn_status st = device_state(&dev);
+    if (st != ATTN_OK) return st;
+    const cudaError_t e = launch_vector_add(a, b, c, n, stream);
+    return e == cudaSuccess ? ATTN_OK : fail("vector_add launch", e);
+}
+
 // --------------------------------------------------------------------------------------------
 // The wait self-test kernel: one thread waits on an mbarrier that nothing arrives on.
 namespace attn {

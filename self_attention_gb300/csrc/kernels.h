@@ -35,6 +35,8 @@ cudaError_t launch_fwd(const FwdArgs &a, cudaStream_t stream);
 cudaError_t launch_bwd_preprocess(const BwdArgs &a, cudaStream_t stream);
 cudaError_t launch_bwd_main(const BwdArgs &a, cudaStream_t stream);
 cudaError_t launch_bwd_convert(const BwdArgs &a, cudaStream_t stream);
+cudaError_t launch_vector_add(const float *a, const float *b, float *c, long long n,
+                              cudaStream_t stream);
 cudaError_t launch_wait_selftest(int *status, uint64_t limit_ns, cudaStream_t stream);
 
 }  // namespace attn

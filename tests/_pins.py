@@ -268,6 +268,27 @@ def pin_rows_variants(lib):
     np.testing.assert_allclose(dv, g["dv"][0, 0, krows], rtol=0, atol=1e-12)
 
 
+def pin_vector_add(lib):
+    """Section 2's C = A + B in fp32: adding zero changes nothing, the sum is symmetric, small
+    integers add exactly, x + (-x) = 0, and a tie rounds to the even neighbour
+    (1 + 3 * 2^-24 lies halfway between 1 + 2^-23 and 1 + 2^-22 and must give 1 + 2^-22)."""
+    rng = _rng(15)
+    a = (rng.standard_normal(1001) * 3).astype(np.float32)
+    b = (rng.standard_normal(1001) * 3).astype(np.float32)
+    zero = np.zeros_like(a)
+    np.testing.assert_array_equal(oracle.vector_add(a, zero, lib=lib), a)
+    np.testing.assert_array_equal(oracle.vector_add(a, b, lib=lib), oracle.vector_add(b, a, lib=lib))
+    i = np.arange(-500, 501, dtype=np.float32)
+    np.testing.assert_array_equal(oracle.vector_add(i, 2 * i, lib=lib), 3 * i)
+    np.testing.assert_array_equal(oracle.vector_add(a, -a, lib=lib), zero)
+    one = np.ones(4, np.float32)
+    tie = np.full(4, 3.0 * 2.0 ** -24, np.float32)
+    np.testing.assert_array_equal(oracle.vector_add(one, tie, lib=lib),
+                                  np.full(4, 1.0 + 2.0 ** -22, np.float32))
+    big = np.full(3, 2.0 ** 24, np.float32)
+    np.testing.assert_array_equal(oracle.vector_add(big, np.ones(3, np.float32), lib=lib), big)
+
+
 ALL_PINS = [
     pin_rows_sum_to_one,
     pin_probabilities_match_library_softmax,
@@ -284,4 +305,5 @@ ALL_PINS = [
     pin_backward_identities,
     pin_library_autograd,
     pin_rows_variants,
+    pin_vector_add,
 ]

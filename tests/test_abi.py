@@ -21,20 +21,21 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(attn_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"^\s*(?:attn_status|size_t|const char \*)\s*(\w+)\s*\(", text,
+                                 flags=re.M)))
 
 
 def test_header_declares_the_boundary():
     names = declared_functions()
     for required in ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_get_device_status",
-                     "attn_status_string"):
+                     "attn_status_string", "vector_add", "attn_bwd_noalloc"):
         assert required in names
 
 
 def test_library_exports_every_declared_symbol(lib):
     out = subprocess.run(["nm", "-D", "--defined-only", build()], capture_output=True,
                          text=True).stdout
-    exported = set(re.findall(r"\bT (attn_\w+)$", out, flags=re.M))
+    exported = set(re.findall(r"\bT (\w+)$", out, flags=re.M))
     for name in declared_functions():
         assert name in exported, f"{name} declared in attn.h but not exported"
         assert hasattr(lib, name)
@@ -108,3 +109,11 @@ def test_bwd_argument_errors(lib):
 def test_debug_timeout_argument_range(lib):
     assert lib.attn_debug_wait_timeout(0, None) == 1
     assert lib.attn_debug_wait_timeout(10 ** 7, None) == 1
+
+
+def test_vector_add_argument_errors(lib):
+    assert lib.vector_add(Q, K, V, -1, None) == 1
+    assert lib.vector_add(Q, K, V, 0, None) == 0          # nothing to do
+    assert lib.vector_add(0, K, V, 16, None) == 1
+    assert lib.vector_add(Q + 4, K, V, 16, None) == 3
+    assert lib.vector_add(Q, K, Q + 16, 16, None) == 1    # partial overlap with an input

@@ -28,6 +28,9 @@ MUTANTS = [
      "const double dpij = dot(doh + i * d, qh + j * d, d);", 0),
     ("rows_lse_missing_max", "return m + log(sum);", "return log(sum) + 0.0 * m;", 0),
     ("rows_bwd_dv_uses_ds", "rv[c] += pij * dout[i * d + c];", "rv[c] += dsij * dout[i * d + c];", 0),
+    ("vector_sub", "c[i] = a[i] + b[i];", "c[i] = a[i] - b[i];", 0),
+    ("vector_twice_a", "c[i] = a[i] + b[i];", "c[i] = a[i] + a[i];", 0),
+    ("vector_in_double_then_halfway_up", "c[i] = a[i] + b[i];", "c[i] = (float)((double)a[i] + (double)b[i] + 1e-30);", 0),
 ]
 
 
