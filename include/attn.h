@@ -90,6 +90,20 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
                      float scale, cudaStream_t stream);
 
 /*
+ * The same backward pass with dQ computed without atomics, so that dQ, dK and dV are bitwise
+ * reproducible from run to run (the article leaves the scheduling of the recomputation open;
+ * this is the alternative to accumulating dQ with fp32 atomics).  Arguments, layouts, workspace
+ * and errors are those of attn_bwd().  It runs the preprocess, the key-stationary kernel for dK
+ * and dV alone, then a query-stationary pass that recomputes S = scale Q K^T and dP = dO V^T
+ * tile by tile and accumulates dQ = scale * dS K in order, one CTA per 128 query rows.  It does
+ * 14 instead of 10 B*H*N^2*d_k flops.
+ */
+attn_status attn_bwd_deterministic(const void *q, const void *k, const void *v, const void *o,
+                                   const void *dout, const float *lse, void *dq, void *dk,
+                                   void *dv, void *workspace, size_t workspace_bytes, int B,
+                                   int H, int N, int d_k, float scale, cudaStream_t stream);
+
+/*
  * The three stream-ordered phases attn_bwd() runs, for callers that schedule or time them
  * separately.  Run on one stream, in this order, with the same sizes, scale and workspace,
  * they produce exactly what attn_bwd() produces.

@@ -26,7 +26,7 @@ __all__ = [
     "AttnError", "attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess",
     "attn_bwd_main", "attn_bwd_dq_convert", "attn_get_device_status",
     "attn_status_string", "attn_last_error_string", "attn_debug_wait_timeout", "attn_bwd_noalloc",
-    "vector_add",
+    "vector_add", "attn_bwd_deterministic",
     "forward", "backward", "attention",
     "load_library", "STATUS",
 ]
@@ -38,7 +38,8 @@ STATUS = {
 }
 EXPORTS = ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess",
            "attn_bwd_main", "attn_bwd_dq_convert", "attn_get_device_status", "attn_status_string",
-           "attn_last_error_string", "attn_debug_wait_timeout", "attn_bwd_noalloc", "vector_add")
+           "attn_last_error_string", "attn_debug_wait_timeout", "attn_bwd_noalloc", "vector_add",
+           "attn_bwd_deterministic")
 
 
 class AttnError(RuntimeError):
@@ -82,6 +83,8 @@ def load_library(path: str = LIB_PATH):
     lib.attn_status_string.restype = ctypes.c_char_p
     lib.attn_last_error_string.argtypes = []
     lib.attn_last_error_string.restype = ctypes.c_char_p
+    lib.attn_bwd_deterministic.argtypes = [_VP] * 10 + [_SZ] + [_I] * 4 + [_F, _VP]
+    lib.attn_bwd_deterministic.restype = _I
     lib.vector_add.argtypes = [_VP, _VP, _VP, ctypes.c_longlong, _VP]
     lib.vector_add.restype = _I
     lib.attn_bwd_noalloc.argtypes = [_VP] * 9 + [_I] * 4 + [_F, _VP]
@@ -178,6 +181,15 @@ def vector_add(a, b, c, n: int, stream=None):
            "vector_add")
 
 
+def attn_bwd_deterministic(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes: int,
+                           B: int, H: int, N: int, d_k: int, scale: float, stream=None):
+    """attn_bwd with dQ computed without atomics: bitwise reproducible dQ, dK, dV."""
+    _raise(load_library().attn_bwd_deterministic(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+        _ptr(workspace), int(workspace_bytes), B, H, N, d_k, float(scale), _stream(stream)),
+        "attn_bwd_deterministic")
+
+
 def attn_get_device_status(stream=None) -> int:
     """Synchronise the stream, then read and clear the device status word (0 = ATTN_OK)."""
     return int(load_library().attn_get_device_status(_stream(stream)))
@@ -211,16 +223,18 @@ def forward(q, k, v, scale: float | None = None, stream=None):
     return o, lse
 
 
-def backward(q, k, v, o, dout, lse, scale: float | None = None, stream=None, workspace=None):
-    """Returns (dq, dk, dv) bf16 for the loss gradient dout = dL/dO."""
+def backward(q, k, v, o, dout, lse, scale: float | None = None, stream=None, workspace=None,
+             deterministic: bool = False):
+    """Returns (dq, dk, dv) bf16 for the loss gradient dout = dL/dO.  deterministic=True uses
+    attn_bwd_deterministic (no atomics; bitwise reproducible)."""
     B, H, N, D = _check_inputs(q, k, v, o, dout)
     scale = 1.0 / math.sqrt(D) if scale is None else scale
     nbytes = attn_bwd_workspace_size(B, H, N, D)
     if workspace is None:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace.numel(), B, H, N, D, scale,
-             stream)
+    fn = attn_bwd_deterministic if deterministic else attn_bwd
+    fn(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace.numel(), B, H, N, D, scale, stream)
     return dq, dk, dv
 
 

@@ -323,6 +323,25 @@ extern "C" attn_status attn_bwd(const void *q, const void *k, const void *v, con
     return e == cudaSuccess ? ATTN_OK : fail("attn_bwd launch", e);
 }
 
+extern "C" attn_status attn_bwd_deterministic(const void *q, const void *k, const void *v,
+                                              const void *o, const void *dout, const float *lse,
+                                              void *dq, void *dk, void *dv, void *workspace,
+                                              size_t workspace_bytes, int B, int H, int N, int d_k,
+                                              float scale, cudaStream_t stream)
+{
+    BwdArgs a;
+    attn_status st = prepare_bwd(a, kPre | kMain | kConv, q, k, v, o, dout, lse, dq, dk, dv,
+                                 workspace, workspace_bytes, B, H, N, d_k, scale);
+    if (st != ATTN_OK) return st;
+    CUresult r;
+    const int bh = B * H;
+    if ((r = make_map(&a.tm_k64, k, bh, N, d_k, 64)) != CUDA_SUCCESS ||
+        (r = make_map(&a.tm_v64, v, bh, N, d_k, 64)) != CUDA_SUCCESS)
+        return fail_driver("cuTensorMapEncodeTiled", r);
+    const cudaError_t e = launch_bwd_deterministic(a, stream);
+    return e == cudaSuccess ? ATTN_OK : fail("attn_bwd_deterministic launch", e);
+}
+
 extern "C" attn_status attn_get_device_status(cudaStream_t stream)
 {
     DeviceState *dev = nullptr;

@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(256)
     bwd_preprocess_kernel(const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restrict__ dout,
                           const float *__restrict__ lse, float *__restrict__ dvec,
                           float *__restrict__ lse2, float *__restrict__ dq_acc, int bh, int n,
-                          int n_pad)
+                          int n_pad, int zero_acc)
 {
     constexpr int TPR = D / 8;  // threads per row, 8 bf16 (16 bytes) each
     const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -101,6 +101,7 @@ __global__ void __launch_bounds__(256)
             lse2[prow] = i < n ? lse[row] * kLog2e : INFINITY;
         }
     }
+    if (!zero_acc) return;
     float4 *acc4 = reinterpret_cast<float4 *>(dq_acc);
     const long long n4 = (long long)bh * n * D / 4;
     for (long long t = tid; t < n4; t += nthreads) acc4[t] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -126,7 +127,7 @@ __global__ void __launch_bounds__(256)
 }
 
 // ------------------------------------------------------------------ 2. main
-template <int D>
+template <int D, bool WITH_DQ>
 __global__ void __launch_bounds__(448, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -287,8 +288,10 @@ __global__ void __launch_bounds__(448, 1)
                 wait_bounded(&bar_ds_full[b], (it >> 1) & 1, g);
                 ptx::tc_fence_after();
                 issue_dv(s, b, it > 0);
-                issue_dq(b);
-                ptx::mma_commit(&bar_dq_full[b]);
+                if constexpr (WITH_DQ) {
+                    issue_dq(b);
+                    ptx::mma_commit(&bar_dq_full[b]);
+                }
                 issue_dk(s, b, it > 0);
                 ptx::mma_commit(&bar_qe[s]);
                 ptx::mma_commit(&bar_ds_empty[b]);
@@ -297,7 +300,8 @@ __global__ void __launch_bounds__(448, 1)
                     wait_bounded(&bar_qf[s2], ((it + 2) / C::QST) & 1, g);
                     ptx::tc_fence_after();
                     issue_dp(s2, b);
-                    wait_bounded(&bar_dq_empty[b], (it >> 1) & 1, g);   // dQ_i^T drained
+                    if constexpr (WITH_DQ)
+                        wait_bounded(&bar_dq_empty[b], (it >> 1) & 1, g);   // dQ_i^T drained
                     ptx::tc_fence_after();
                     issue_s(s2, b);
                     ptx::mma_commit(&bar_sdp[b]);
@@ -408,7 +412,7 @@ __global__ void __launch_bounds__(448, 1)
         const int r = (warp - 8) * 32 + lane;   // d column = TMEM lane of dQ^T
         const uint32_t lane_off = (uint32_t)((warp - 8) * 32) << 16;
         const bool leader = threadIdx.x == 256;
-        for (int it = 0; it < nq; ++it) {
+        for (int it = 0; it < (WITH_DQ ? nq : 0); ++it) {
             const int b = it & 1;
             wait_bounded(&bar_dq_full[b], (it >> 1) & 1, g);
             ptx::tc_fence_after();
@@ -458,6 +462,251 @@ __global__ void __launch_bounds__(448, 1)
     }
 }
 
+// ------------------------------------------------------------------ 4. deterministic dQ pass
+// dQ_i = scale * sum_j dS_ij K_j without atomics: one CTA owns 128 query rows of one head and
+// walks the key tiles (64 keys each) in order, recomputing S = Q K^T and dP = dO V^T on chip.
+//   warp 8      TMA: Q_i and dO_i once; a ring of (K_j, V_j).
+//   warp 9      tcgen05: S_j, dP_j into TMEM (two buffers), then dQ += dS_j K_j with dS_j read
+//               from TMEM (bf16, written over S_j) and K_j MN-major from shared memory.
+//   warps 0-7   two warpgroups, alternating key tiles; thread = query row, whose LSE and D
+//               sit in registers: P = 2^(S c - LSE log2 e), dS = P o (dP - D).
+// TMEM: S_0 [0,64), dP_0 [64,128), S_1 [128,192), dP_1 [192,256), dQ [256,256+d).
+template <int D>
+struct DqCfg {
+    static constexpr int BM = 128;   // query rows per CTA
+    static constexpr int BN = 64;    // keys per step
+    static constexpr int STAGES = (D == 64) ? 6 : 4;
+    static constexpr int Q_BYTES = BM * D * 2;
+    static constexpr int KV_BYTES = BN * D * 2;
+    static constexpr int STAGE_BYTES = 2 * KV_BYTES;   // K_j then V_j
+    static constexpr int SMEM_BYTES = 2 * Q_BYTES + STAGES * STAGE_BYTES + 1024;
+    static constexpr int THREADS = 320;
+    static constexpr uint32_t TM_DQ = 256;
+    __host__ __device__ static constexpr uint32_t tm_s(int b) { return b * 128; }
+    __host__ __device__ static constexpr uint32_t tm_dp(int b) { return b * 128 + 64; }
+};
+
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                  const __grid_constant__ CUtensorMap tm_k64, const __grid_constant__ CUtensorMap tm_v64,
+                  const float *__restrict__ lse2, const float *__restrict__ dvec,
+                  __nv_bfloat16 *__restrict__ dq, int n, int n_pad, int n_qblocks, float scale,
+                  int *status)
+{
+    using C = DqCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    uint8_t *sQ = smem;                      // Q_i: two 64-column halves of 128 rows
+    uint8_t *sdO = sQ + C::Q_BYTES;          // dO_i, same layout
+    uint8_t *sKV = sdO + C::Q_BYTES;         // STAGES x {K_j, V_j}
+
+    __shared__ uint64_t bar_q, bar_kvf[C::STAGES], bar_kve[C::STAGES];
+    __shared__ uint64_t bar_sdp[2], bar_ds[2], bar_dq, bar_done;
+    __shared__ uint32_t tmem_sh;
+    __shared__ int abort_sh;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.x / n_qblocks;
+    const int q0 = (blockIdx.x % n_qblocks) * C::BM;
+    const int nk = (n + C::BN - 1) / C::BN;
+    const Guard g{&abort_sh, status, kWaitLimitNs};
+
+    if (threadIdx.x == 0) {
+        abort_sh = 0;
+        ptx::mbar_init(&bar_q, 1);
+        for (int s = 0; s < C::STAGES; ++s) {
+            ptx::mbar_init(&bar_kvf[s], 1);
+            ptx::mbar_init(&bar_kve[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(&bar_sdp[b], 1);
+            ptx::mbar_init(&bar_ds[b], 128);
+        }
+        ptx::mbar_init(&bar_dq, 1);
+        ptx::mbar_init(&bar_done, 1);
+        ptx::fence_mbar_init();
+    }
+    if (warp == 9) {
+        ptx::tmem_alloc(&tmem_sh, 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = tmem_sh;
+
+    if (warp == 8) {
+        // ---------------------------------------------------------------- TMA producer
+        if (ptx::elect_one()) {
+            ptx::tma_prefetch_desc(&tm_q);
+            ptx::tma_prefetch_desc(&tm_do);
+            ptx::tma_prefetch_desc(&tm_k64);
+            ptx::tma_prefetch_desc(&tm_v64);
+            ptx::mbar_arrive_expect_tx(&bar_q, 2 * C::Q_BYTES);
+            for (int h = 0; h < D / 64; ++h)
+                for (int rb = 0; rb < 2; ++rb) {
+                    ptx::tma_load_3d(sQ + h * C::BM * 128 + rb * 8192, &tm_q, &bar_q, h * 64, q0 + rb * 64, bh);
+                    ptx::tma_load_3d(sdO + h * C::BM * 128 + rb * 8192, &tm_do, &bar_q, h * 64, q0 + rb * 64, bh);
+                }
+            for (int j = 0; j < nk; ++j) {
+                const int s = j % C::STAGES;
+                const uint32_t ph = (j / C::STAGES) & 1;
+                wait_bounded(&bar_kve[s], ph ^ 1, g);
+                ptx::mbar_arrive_expect_tx(&bar_kvf[s], C::STAGE_BYTES);
+                uint8_t *stage = sKV + s * C::STAGE_BYTES;
+                for (int h = 0; h < D / 64; ++h) {
+                    ptx::tma_load_3d(stage + h * C::BN * 128, &tm_k64, &bar_kvf[s], h * 64, j * C::BN, bh);
+                    ptx::tma_load_3d(stage + C::KV_BYTES + h * C::BN * 128, &tm_v64, &bar_kvf[s],
+                                     h * 64, j * C::BN, bh);
+                }
+            }
+            wait_bounded(&bar_q, 0, g);
+            for (int j = (nk > C::STAGES ? nk - C::STAGES : 0); j < nk; ++j)
+                wait_bounded(&bar_kvf[j % C::STAGES], (j / C::STAGES) & 1, g);
+        }
+    } else if (warp == 9) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (ptx::elect_one()) {
+            const uint32_t idSP = ptx::idesc_bf16_f32(128, C::BN, false, false);
+            const uint32_t idQ = ptx::idesc_bf16_f32(128, D, false, true);
+            const uint32_t q_base = ptx::smem_u32(sQ), do_base = ptx::smem_u32(sdO),
+                           kv_base = ptx::smem_u32(sKV);
+            auto kst = [&](int s) { return kv_base + s * C::STAGE_BYTES; };
+            // S_j = Q K_j^T and dP_j = dO V_j^T: all operands K-major over d.
+            auto issue_sdp = [&](int s, int b) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t offa = (kk >> 2) * (C::BM * 128) + (kk & 3) * 32;
+                    const uint32_t offb = (kk >> 2) * (C::BN * 128) + (kk & 3) * 32;
+                    ptx::mma_ss(tmem + C::tm_s(b), ptx::sdesc_sw128(q_base + offa, 16, 1024),
+                                ptx::sdesc_sw128(kst(s) + offb, 16, 1024), idSP, kk > 0 ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t offa = (kk >> 2) * (C::BM * 128) + (kk & 3) * 32;
+                    const uint32_t offb = (kk >> 2) * (C::BN * 128) + (kk & 3) * 32;
+                    ptx::mma_ss(tmem + C::tm_dp(b), ptx::sdesc_sw128(do_base + offa, 16, 1024),
+                                ptx::sdesc_sw128(kst(s) + C::KV_BYTES + offb, 16, 1024), idSP,
+                                kk > 0 ? 1u : 0u);
+                }
+            };
+            // dQ += dS_j K_j: A = dS_j (TMEM, 8 columns per 16 keys), B = K_j MN-major
+            // (K = keys, N = d; 64-column halves BN*128 bytes apart).
+            auto issue_dq = [&](int s, int b, bool acc) {
+#pragma unroll
+                for (int kk = 0; kk < C::BN / 16; ++kk)
+                    ptx::mma_ts(tmem + C::TM_DQ, tmem + C::tm_s(b) + kk * 8,
+                                ptx::sdesc_sw128(kst(s) + kk * 2048, C::BN * 128, 1024), idQ,
+                                (acc || kk > 0) ? 1u : 0u);
+            };
+            wait_bounded(&bar_q, 0, g);
+            for (int j = 0; j < 2 && j < nk; ++j) {
+                wait_bounded(&bar_kvf[j % C::STAGES], (j / C::STAGES) & 1, g);
+                ptx::tc_fence_after();
+                issue_sdp(j % C::STAGES, j);
+                ptx::mma_commit(&bar_sdp[j]);
+            }
+            for (int j = 0; j < nk; ++j) {
+                const int b = j & 1, s = j % C::STAGES;
+                wait_bounded(&bar_ds[b], (j >> 1) & 1, g);
+                ptx::tc_fence_after();
+                issue_dq(s, b, j > 0);
+                ptx::mma_commit(&bar_kve[s]);
+                if (j + 2 < nk) {
+                    const int s2 = (j + 2) % C::STAGES;
+                    wait_bounded(&bar_kvf[s2], ((j + 2) / C::STAGES) & 1, g);
+                    ptx::tc_fence_after();
+                    issue_sdp(s2, b);
+                    ptx::mma_commit(&bar_sdp[b]);
+                }
+            }
+            ptx::mma_commit(&bar_dq);
+            ptx::mma_commit(&bar_done);
+            wait_bounded(&bar_done, 0, g);
+        }
+    } else {
+        // ---------------------------------------------------------------- P / dS warpgroups
+        const int wg = warp >> 2, cw = warp & 3;
+        const int row = q0 + cw * 32 + lane;    // query row = TMEM lane
+        const bool row_ok = row < n;
+        const uint32_t lane_off = (uint32_t)(cw * 32) << 16;
+        const float scale_log2 = scale * kLog2e;
+        const float l2 = row_ok ? lse2[(size_t)bh * n_pad + row] : INFINITY;
+        const float dr = row_ok ? dvec[(size_t)bh * n_pad + row] : 0.f;
+        for (int j = wg; j < nk; j += 2) {
+            const int b = wg;
+            wait_bounded(&bar_sdp[b], (j >> 1) & 1, g);
+            ptx::tc_fence_after();
+            const int valid = n - j * C::BN;   // keys of this tile below n
+            const uint32_t tS = tmem + lane_off + C::tm_s(b), tDP = tmem + lane_off + C::tm_dp(b);
+            // 16 keys at a time; dS of quarter q goes to columns [8q, 8q + 8), over S already read
+            uint32_t sv[2][16], dpv[2][16];
+            ptx::tmem_ld16(tS, sv[0]);
+            ptx::tmem_ld16(tDP, dpv[0]);
+            ptx::tmem_ld_wait();
+            reg_fence(sv[0]);
+            reg_fence(dpv[0]);
+#pragma unroll
+            for (int qt = 0; qt < 4; ++qt) {
+                const int cur = qt & 1;
+                if (qt < 3) {
+                    ptx::tmem_ld16(tS + (qt + 1) * 16, sv[cur ^ 1]);
+                    ptx::tmem_ld16(tDP + (qt + 1) * 16, dpv[cur ^ 1]);
+                }
+                uint32_t dsp[8];
+#pragma unroll
+                for (int c = 0; c < 16; c += 2) {
+                    float p0 = ptx::ex2(fmaf(__uint_as_float(sv[cur][c]), scale_log2, -l2));
+                    float p1 = ptx::ex2(fmaf(__uint_as_float(sv[cur][c + 1]), scale_log2, -l2));
+                    if (qt * 16 + c >= valid) p0 = 0.f;
+                    if (qt * 16 + c + 1 >= valid) p1 = 0.f;
+                    dsp[c / 2] = ptx::pack_bf16x2(p0 * (__uint_as_float(dpv[cur][c]) - dr),
+                                                  p1 * (__uint_as_float(dpv[cur][c + 1]) - dr));
+                }
+                ptx::tmem_st8(tS + qt * 8, dsp);
+                if (qt < 3) {
+                    ptx::tmem_ld_wait();
+                    reg_fence(sv[cur ^ 1]);
+                    reg_fence(dpv[cur ^ 1]);
+                }
+            }
+            ptx::tmem_st_wait();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&bar_ds[b]);
+        }
+        // epilogue: dQ = scale * acc in bf16; warpgroup wg writes columns [wg*D/2, (wg+1)*D/2)
+        wait_bounded(&bar_dq, 0, g);
+        ptx::tc_fence_after();
+        __nv_bfloat16 *dst_row = dq + ((size_t)bh * n + (row_ok ? row : 0)) * D;
+#pragma unroll
+        for (int c = 0; c < D / 2; c += 32) {
+            const int col = wg * (D / 2) + c;
+            uint32_t v[32];
+            ptx::tmem_ld32(tmem + lane_off + C::TM_DQ + col, v);
+            ptx::tmem_ld_wait();
+            reg_fence(v);
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+                pk[e] = ptx::pack_bf16x2(__uint_as_float(v[2 * e]) * scale, __uint_as_float(v[2 * e + 1]) * scale);
+            if (row_ok) {
+                uint4 *dst = reinterpret_cast<uint4 *>(dst_row + col);
+#pragma unroll
+                for (int v4 = 0; v4 < 4; ++v4)
+                    dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+            }
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 9) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 512);
+    }
+}
+
 int g_num_sms = 0;
 
 int elementwise_blocks()
@@ -472,24 +721,24 @@ int elementwise_blocks()
 }
 
 template <int D>
-cudaError_t launch_preprocess_d(const BwdArgs &a, cudaStream_t stream)
+cudaError_t launch_preprocess_d(const BwdArgs &a, bool zero_acc, cudaStream_t stream)
 {
     bwd_preprocess_kernel<D><<<elementwise_blocks(), 256, 0, stream>>>(
         reinterpret_cast<const __nv_bfloat16 *>(a.o), reinterpret_cast<const __nv_bfloat16 *>(a.dout),
-        a.lse, a.dvec, a.lse2, a.dq_acc, a.bh, a.n, a.n_pad);
+        a.lse, a.dvec, a.lse2, a.dq_acc, a.bh, a.n, a.n_pad, zero_acc ? 1 : 0);
     return cudaGetLastError();
 }
 
-template <int D>
+template <int D, bool WITH_DQ>
 cudaError_t launch_main_d(const BwdArgs &a, cudaStream_t stream)
 {
     using C = BwdCfg<D>;
-    cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel<D, WITH_DQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int n_kvblocks = (a.n + C::BN - 1) / C::BN;
     const long long ctas = (long long)n_kvblocks * a.bh;
-    bwd_main_kernel<D><<<(unsigned)ctas, C::THREADS, C::SMEM_BYTES, stream>>>(
+    bwd_main_kernel<D, WITH_DQ><<<(unsigned)ctas, C::THREADS, C::SMEM_BYTES, stream>>>(
         a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse2, a.dvec, a.dq_acc,
         reinterpret_cast<__nv_bfloat16 *>(a.dk), reinterpret_cast<__nv_bfloat16 *>(a.dv), a.n,
         a.n_pad, n_kvblocks, a.scale, a.status);
@@ -500,12 +749,37 @@ cudaError_t launch_main_d(const BwdArgs &a, cudaStream_t stream)
 
 cudaError_t launch_bwd_preprocess(const BwdArgs &a, cudaStream_t stream)
 {
-    return a.d == 64 ? launch_preprocess_d<64>(a, stream) : launch_preprocess_d<128>(a, stream);
+    return a.d == 64 ? launch_preprocess_d<64>(a, true, stream) : launch_preprocess_d<128>(a, true, stream);
 }
 
 cudaError_t launch_bwd_main(const BwdArgs &a, cudaStream_t stream)
 {
-    return a.d == 64 ? launch_main_d<64>(a, stream) : launch_main_d<128>(a, stream);
+    return a.d == 64 ? launch_main_d<64, true>(a, stream) : launch_main_d<128, true>(a, stream);
+}
+
+template <int D>
+cudaError_t launch_dq_d(const BwdArgs &a, cudaStream_t stream)
+{
+    using C = DqCfg<D>;
+    cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int n_qblocks = (a.n + C::BM - 1) / C::BM;
+    const long long ctas = (long long)n_qblocks * a.bh;
+    bwd_dq_kernel<D><<<(unsigned)ctas, C::THREADS, C::SMEM_BYTES, stream>>>(
+        a.tm_q, a.tm_do, a.tm_k64, a.tm_v64, a.lse2, a.dvec,
+        reinterpret_cast<__nv_bfloat16 *>(a.dq), a.n, a.n_pad, n_qblocks, a.scale, a.status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_deterministic(const BwdArgs &a, cudaStream_t stream)
+{
+    cudaError_t e = a.d == 64 ? launch_preprocess_d<64>(a, false, stream)
+                              : launch_preprocess_d<128>(a, false, stream);
+    if (e == cudaSuccess)
+        e = a.d == 64 ? launch_main_d<64, false>(a, stream) : launch_main_d<128, false>(a, stream);
+    if (e == cudaSuccess) e = a.d == 64 ? launch_dq_d<64>(a, stream) : launch_dq_d<128>(a, stream);
+    return e;
 }
 
 cudaError_t launch_bwd_convert(const BwdArgs &a, cudaStream_t stream)

@@ -19,6 +19,7 @@ struct FwdArgs {
 
 struct BwdArgs {
     CUtensorMap tm_q, tm_k, tm_v, tm_do;
+    CUtensorMap tm_k64, tm_v64;     // K and V with 64-row boxes (deterministic dQ pass only)
     const void *o, *dout;           // [BH, N, d] bf16
     const float *lse;               // [BH, N]
     void *dq, *dk, *dv;             // [BH, N, d] bf16
@@ -35,6 +36,9 @@ cudaError_t launch_fwd(const FwdArgs &a, cudaStream_t stream);
 cudaError_t launch_bwd_preprocess(const BwdArgs &a, cudaStream_t stream);
 cudaError_t launch_bwd_main(const BwdArgs &a, cudaStream_t stream);
 cudaError_t launch_bwd_convert(const BwdArgs &a, cudaStream_t stream);
+// The deterministic backward: preprocess (no accumulator), the main kernel without its dQ part,
+// then a query-stationary pass that computes dQ without atomics.
+cudaError_t launch_bwd_deterministic(const BwdArgs &a, cudaStream_t stream);
 cudaError_t launch_vector_add(const float *a, const float *b, float *c, long long n,
                               cudaStream_t stream);
 cudaError_t launch_wait_selftest(int *status, uint64_t limit_ns, cudaStream_t stream);

@@ -190,3 +190,65 @@ def test_bwd_phases_match_single_call():
     assert sa.attn_get_device_status() == 0
     assert torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
     check_grad("dq", dq2.float().cpu().numpy(), dq1.double().cpu().numpy(), "phases")
+
+
+# ------------------------------------------------------------------ deterministic dQ pass
+def run_det(inp, scale):
+    q, k, v, do = (inp[x].cuda() for x in ("q", "k", "v", "do"))
+    B, H, N, D = q.shape
+    o, lse = sa.forward(q, k, v, scale)
+    bufs = [_guarded((B, H, N, D), torch.bfloat16) for _ in range(3)]
+    dq, dk, dv = (b[1] for b in bufs)
+    ws_bytes = sa.attn_bwd_workspace_size(B, H, N, D)
+    ws = torch.full((ws_bytes,), 0x7F, dtype=torch.uint8, device="cuda")
+    sa.attn_bwd_deterministic(q, k, v, o, do, lse, dq, dk, dv, ws, ws_bytes, B, H, N, D, scale)
+    assert sa.attn_get_device_status() == 0
+    assert all(_intact(b[0]) for b in bufs), "a store escaped a gradient tensor"
+    to = lambda t: t.float().cpu().numpy()
+    return {"dq": to(dq), "dk": to(dk), "dv": to(dv)}
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("n", [1, 2, 63, 64, 65, 129, 196, 257, 1000])
+def test_det_edge_sizes(n, d):
+    inp = make_qkv(1, 3, n, d, seed=9500 + n + d)
+    scale = 1.0 / math.sqrt(d)
+    got = run_det(inp, scale)
+    ref = oracle.bwd(inp["q"], inp["k"], inp["v"], inp["do"], scale)
+    for name in ("dq", "dk", "dv"):
+        if n == 1 and name in ("dq", "dk"):
+            assert np.abs(got[name]).max() <= 1e-6
+            continue
+        check_grad(name, got[name], ref[name], f"deterministic N={n} d={d}")
+
+
+def test_det_bitwise_repeatable_and_close_to_atomic():
+    inp = make_qkv(2, 3, 900, 128, seed=41, qk_std=2.0)
+    a, b = run_det(inp, 0.0884), run_det(inp, 0.0884)
+    for name in ("dq", "dk", "dv"):
+        np.testing.assert_array_equal(a[name], b[name])
+    atomic = run_fwd_bwd(inp, 0.0884)
+    np.testing.assert_array_equal(a["dk"], atomic["dk"])
+    np.testing.assert_array_equal(a["dv"], atomic["dv"])
+    check_grad("dq", a["dq"], atomic["dq"].astype(np.float64), "deterministic vs atomic")
+
+
+@pytest.mark.parametrize("name", ["vit_b16_batch", "long_text"])
+def test_det_workloads(name):
+    w = WORKLOADS[name]
+    inp = make_workload_inputs(w)
+    got = run_det(inp, w.scale)
+    if name == "vit_b16_batch":
+        ref = oracle.bwd(inp["q"], inp["k"], inp["v"], inp["do"], w.scale)
+        for n_ in ("dq", "dk", "dv"):
+            check_grad(n_, got[n_], ref[n_], name)
+        return
+    rng = np.random.default_rng(3)
+    b, h = 0, w.H - 1
+    qrows = np.unique(np.concatenate([[0, w.N - 1], rng.integers(0, w.N, 40)]))
+    krows = np.unique(np.concatenate([[0, w.N - 1], rng.integers(0, w.N, 40)]))
+    dq, dk, dv = oracle.bwd_rows(inp["q"][b, h], inp["k"][b, h], inp["v"][b, h], inp["do"][b, h],
+                                 qrows, krows, w.scale)
+    check_grad("dq", got["dq"][b, h, qrows], dq, name)
+    check_grad("dk", got["dk"][b, h, krows], dk, name)
+    check_grad("dv", got["dv"][b, h, krows], dv, name)
