@@ -151,6 +151,34 @@ const char *attn_last_error_string(void);
 attn_status attn_debug_wait_timeout(unsigned limit_us, cudaStream_t stream);
 
 /*
+ * Query / key / value projection (section 1, "Generating queries, keys and values":
+ * Q = X W_Q, K = X W_K, V = X W_V, each W in R^(D x d_k) per head): the step that feeds
+ * attn_fwd.  The heads' weights side by side form one D x D matrix per projection; head h
+ * takes its columns [h d_k, (h+1) d_k), and the outputs are written directly in the
+ * [B, H, N, d_k] layout attn_fwd reads.
+ *   x             : [B, N, D] bf16 (token rows).
+ *   w_q, w_k, w_v : [D, D] bf16 row-major (input dimension x output columns).
+ *   q, k, v       : [B, H, N, d_k] bf16 outputs (fp32 accumulation, rounded to nearest).
+ * Requirements: D = H * d_k, D a multiple of 128, d_k in {64, 128}; pointers 16-byte aligned;
+ * outputs overlap neither each other nor the inputs.
+ */
+attn_status attn_qkv_proj(const void *x, const void *w_q, const void *w_k, const void *w_v,
+                          void *q, void *k, void *v, int B, int N, int D, int H, int d_k,
+                          cudaStream_t stream);
+
+/*
+ * Backward of attn_qkv_proj for the gradients dq, dk, dv ([B, H, N, d_k] bf16, e.g. from
+ * attn_bwd): dX = sum_t dY_t W_t^T ([B, N, D] bf16 output) and dW_t = X^T dY_t summed over all
+ * B*N tokens ([D, D] fp32 outputs, written from zero; the token rows are split across CTAs and
+ * their partial sums added with fp32 atomics, so the last bits of dW may vary between runs).
+ * Same size rules as attn_qkv_proj.
+ */
+attn_status attn_qkv_proj_bwd(const void *x, const void *w_q, const void *w_k, const void *w_v,
+                              const void *dq, const void *dk, const void *dv, void *dx,
+                              float *dw_q, float *dw_k, float *dw_v, int B, int N, int D, int H,
+                              int d_k, cudaStream_t stream);
+
+/*
  * Element-wise fp32 addition c[i] = a[i] + b[i], 0 <= i < n: the vector_add_cuda kernel of
  * section 2 ("Practical code comparison: raw CUDA C++ vs OpenAI Triton", the raw CUDA C++
  * version: one element per index, guarded by i < n), used here as the library's HBM bandwidth

@@ -174,3 +174,43 @@ def vector_add(a, b, lib=None):
     fp = ctypes.POINTER(ctypes.c_float)
     lib.oracle_vector_add(a.ctypes.data_as(fp), b.ctypes.data_as(fp), c.ctypes.data_as(fp), a.size)
     return c
+
+
+# ---------------------------------------------------------------- QKV projection
+# "Self-attention, CUDA kernels and FlashAttention", section 1 ("Generating queries, keys and
+# values"): Q = X W_Q, K = X W_K, V = X W_V, with W in R^(D x d_k) per head; the heads' weights
+# side by side form one D x D matrix, head h taking columns [h*d_k, (h+1)*d_k).  Plain fp64 matrix
+# products (numpy) followed by the split of the columns into heads.
+
+def _heads(y, H):
+    """[B, N, D] -> [B, H, N, D/H]: head h = columns [h*d, (h+1)*d)."""
+    B, N, D = y.shape
+    return np.ascontiguousarray(y.reshape(B, N, H, D // H).transpose(0, 2, 1, 3))
+
+
+def _merge(z):
+    """[B, H, N, d] -> [B, N, H*d], the inverse of _heads."""
+    B, H, N, d = z.shape
+    return np.ascontiguousarray(z.transpose(0, 2, 1, 3).reshape(B, N, H * d))
+
+
+def qkv_proj(x, w_q, w_k, w_v, H):
+    """x [B, N, D]; w_* [D, D].  Returns (q, k, v), each [B, H, N, D/H] fp64."""
+    x = _f64(x)
+    return tuple(_heads(x @ _f64(w), H) for w in (w_q, w_k, w_v))
+
+
+def qkv_proj_bwd(x, w_q, w_k, w_v, dq, dk, dv):
+    """Gradients of sum_t <dY_t, Y_t> for Y_t = X W_t (heads merged back into columns):
+    dX = sum_t dY_t W_t^T and dW_t = X^T dY_t (summed over the batch).  Returns
+    (dx [B,N,D], dw_q, dw_k, dw_v [D,D]) in fp64."""
+    x = _f64(x)
+    B, N, D = x.shape
+    xf = x.reshape(B * N, D)
+    dx = np.zeros((B * N, D))
+    dws = []
+    for w, dy in ((w_q, dq), (w_k, dk), (w_v, dv)):
+        g = _merge(_f64(dy)).reshape(B * N, D)
+        dx += g @ _f64(w).T
+        dws.append(xf.T @ g)
+    return (dx.reshape(B, N, D), *dws)

@@ -26,7 +26,8 @@ __all__ = [
     "AttnError", "attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess",
     "attn_bwd_main", "attn_bwd_dq_convert", "attn_get_device_status",
     "attn_status_string", "attn_last_error_string", "attn_debug_wait_timeout", "attn_bwd_noalloc",
-    "vector_add", "attn_bwd_deterministic",
+    "vector_add", "attn_bwd_deterministic", "attn_qkv_proj", "attn_qkv_proj_bwd", "qkv_proj",
+    "qkv_proj_backward",
     "forward", "backward", "attention",
     "load_library", "STATUS",
 ]
@@ -39,7 +40,7 @@ STATUS = {
 EXPORTS = ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess",
            "attn_bwd_main", "attn_bwd_dq_convert", "attn_get_device_status", "attn_status_string",
            "attn_last_error_string", "attn_debug_wait_timeout", "attn_bwd_noalloc", "vector_add",
-           "attn_bwd_deterministic")
+           "attn_bwd_deterministic", "attn_qkv_proj", "attn_qkv_proj_bwd")
 
 
 class AttnError(RuntimeError):
@@ -85,6 +86,10 @@ def load_library(path: str = LIB_PATH):
     lib.attn_last_error_string.restype = ctypes.c_char_p
     lib.attn_bwd_deterministic.argtypes = [_VP] * 10 + [_SZ] + [_I] * 4 + [_F, _VP]
     lib.attn_bwd_deterministic.restype = _I
+    lib.attn_qkv_proj.argtypes = [_VP] * 7 + [_I] * 5 + [_VP]
+    lib.attn_qkv_proj.restype = _I
+    lib.attn_qkv_proj_bwd.argtypes = [_VP] * 11 + [_I] * 5 + [_VP]
+    lib.attn_qkv_proj_bwd.restype = _I
     lib.vector_add.argtypes = [_VP, _VP, _VP, ctypes.c_longlong, _VP]
     lib.vector_add.restype = _I
     lib.attn_bwd_noalloc.argtypes = [_VP] * 9 + [_I] * 4 + [_F, _VP]
@@ -188,6 +193,37 @@ def attn_bwd_deterministic(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspa
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
         _ptr(workspace), int(workspace_bytes), B, H, N, d_k, float(scale), _stream(stream)),
         "attn_bwd_deterministic")
+
+
+def attn_qkv_proj(x, w_q, w_k, w_v, q, k, v, B: int, N: int, D: int, H: int, d_k: int,
+                  stream=None):
+    _raise(load_library().attn_qkv_proj(_ptr(x), _ptr(w_q), _ptr(w_k), _ptr(w_v), _ptr(q), _ptr(k),
+                                        _ptr(v), B, N, D, H, d_k, _stream(stream)), "attn_qkv_proj")
+
+
+def attn_qkv_proj_bwd(x, w_q, w_k, w_v, dq, dk, dv, dx, dw_q, dw_k, dw_v, B: int, N: int, D: int,
+                      H: int, d_k: int, stream=None):
+    _raise(load_library().attn_qkv_proj_bwd(
+        _ptr(x), _ptr(w_q), _ptr(w_k), _ptr(w_v), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dx),
+        _ptr(dw_q), _ptr(dw_k), _ptr(dw_v), B, N, D, H, d_k, _stream(stream)), "attn_qkv_proj_bwd")
+
+
+def qkv_proj(x, w_q, w_k, w_v, H: int, stream=None):
+    """Q, K, V = X W_Q, X W_K, X W_V split into H heads: x [B,N,D] bf16 -> 3 x [B,H,N,D/H] bf16."""
+    B, N, D = x.shape
+    outs = [torch.empty((B, H, N, D // H), dtype=torch.bfloat16, device=x.device) for _ in range(3)]
+    attn_qkv_proj(x, w_q, w_k, w_v, *outs, B, N, D, H, D // H, stream)
+    return tuple(outs)
+
+
+def qkv_proj_backward(x, w_q, w_k, w_v, dq, dk, dv, stream=None):
+    """Returns (dx [B,N,D] bf16, dw_q, dw_k, dw_v [D,D] fp32)."""
+    B, N, D = x.shape
+    H = dq.shape[1]
+    dx = torch.empty_like(x)
+    dws = [torch.empty((D, D), dtype=torch.float32, device=x.device) for _ in range(3)]
+    attn_qkv_proj_bwd(x, w_q, w_k, w_v, dq, dk, dv, dx, *dws, B, N, D, H, D // H, stream)
+    return (dx, *dws)
 
 
 def attn_get_device_status(stream=None) -> int:

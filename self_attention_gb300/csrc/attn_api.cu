@@ -388,6 +388,106 @@ extern "C" attn_status attn_debug_wait_timeout(unsigned limit_us, cudaStream_t s
 
 extern "C" const char *attn_last_error_string(void) { return t_last_error; }
 
+namespace {
+
+attn_status check_proj(const void *x, const void *const w[3], int B, int N, int D, int H, int d_k)
+{
+    if (d_k != 64 && d_k != 128) return ATTN_ERR_UNSUPPORTED_DK;
+    if (B < 1 || N < 1 || H < 1 || D != H * d_k || D % 128 != 0) return ATTN_ERR_INVALID_ARG;
+    if ((long long)B * N * D >= (1LL << 40) || (long long)B * H > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+    if (!x || !w[0] || !w[1] || !w[2]) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w[0]) || !aligned16(w[1]) || !aligned16(w[2])) return ATTN_ERR_MISALIGNED;
+    return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" attn_status attn_qkv_proj(const void *x, const void *w_q, const void *w_k,
+                                     const void *w_v, void *q, void *k, void *v, int B, int N,
+                                     int D, int H, int d_k, cudaStream_t stream)
+{
+    const void *w[3] = {w_q, w_k, w_v};
+    void *out[3] = {q, k, v};
+    attn_status st = check_proj(x, w, B, N, D, H, d_k);
+    if (st != ATTN_OK) return st;
+    const size_t xbytes = (size_t)B * N * D * 2, wbytes = (size_t)D * D * 2;
+    for (int t = 0; t < 3; ++t) {
+        if (!out[t]) return ATTN_ERR_INVALID_ARG;
+        if (!aligned16(out[t])) return ATTN_ERR_MISALIGNED;
+        if (overlap(span(out[t], xbytes), span(x, xbytes))) return ATTN_ERR_INVALID_ARG;
+        for (int u = 0; u < 3; ++u) {
+            if (overlap(span(out[t], xbytes), span(w[u], wbytes))) return ATTN_ERR_INVALID_ARG;
+            if (u > t && overlap(span(out[t], xbytes), span(out[u], xbytes))) return ATTN_ERR_INVALID_ARG;
+        }
+    }
+    DeviceState *dev = nullptr;
+    if ((st = device_state(&dev)) != ATTN_OK) return st;
+    ProjMaps m;
+    std::memset(&m, 0, sizeof m);
+    CUresult r = make_map(&m.a[0], x, 1, B * N, D, 128);            // X as [B*N, D]
+    for (int t = 0; t < 3 && r == CUDA_SUCCESS; ++t) r = make_map(&m.b[t], w[t], 1, D, D, 64);
+    if (r != CUDA_SUCCESS) return fail_driver("cuTensorMapEncodeTiled", r);
+    m.a[1] = m.a[2] = m.a[0];
+    ProjArgs a = {};
+    a.B = B; a.N = N; a.D = D; a.H = H; a.dk = d_k; a.status = dev->status;
+    for (int t = 0; t < 3; ++t) a.qkv[t] = static_cast<__nv_bfloat16 *>(out[t]);
+    const cudaError_t e = launch_proj_fwd(m, a, stream);
+    return e == cudaSuccess ? ATTN_OK : fail("attn_qkv_proj launch", e);
+}
+
+extern "C" attn_status attn_qkv_proj_bwd(const void *x, const void *w_q, const void *w_k,
+                                         const void *w_v, const void *dq, const void *dk,
+                                         const void *dv, void *dx, float *dw_q, float *dw_k,
+                                         float *dw_v, int B, int N, int D, int H, int d_k,
+                                         cudaStream_t stream)
+{
+    const void *w[3] = {w_q, w_k, w_v};
+    const void *dy[3] = {dq, dk, dv};
+    float *dw[3] = {dw_q, dw_k, dw_v};
+    attn_status st = check_proj(x, w, B, N, D, H, d_k);
+    if (st != ATTN_OK) return st;
+    if (!dx) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(dx)) return ATTN_ERR_MISALIGNED;
+    const size_t xbytes = (size_t)B * N * D * 2, wbytes = (size_t)D * D * 2, dwbytes = (size_t)D * D * 4;
+    Range ins[7] = {span(x, xbytes), span(w[0], wbytes), span(w[1], wbytes), span(w[2], wbytes),
+                    span(dy[0], xbytes), span(dy[1], xbytes), span(dy[2], xbytes)};
+    Range outs[4] = {span(dx, xbytes), span(dw[0], dwbytes), span(dw[1], dwbytes), span(dw[2], dwbytes)};
+    for (int t = 0; t < 3; ++t) {
+        if (!dy[t] || !dw[t]) return ATTN_ERR_INVALID_ARG;
+        if (!aligned16(dy[t]) || !aligned16(dw[t])) return ATTN_ERR_MISALIGNED;
+    }
+    for (int i = 0; i < 4; ++i) {
+        for (const Range &r : ins)
+            if (overlap(r, outs[i])) return ATTN_ERR_INVALID_ARG;
+        for (int j = i + 1; j < 4; ++j)
+            if (overlap(outs[i], outs[j])) return ATTN_ERR_INVALID_ARG;
+    }
+    DeviceState *dev = nullptr;
+    if ((st = device_state(&dev)) != ATTN_OK) return st;
+    ProjArgs a = {};
+    a.B = B; a.N = N; a.D = D; a.H = H; a.dk = d_k; a.status = dev->status;
+    a.dx = static_cast<__nv_bfloat16 *>(dx);
+    for (int t = 0; t < 3; ++t) a.dw[t] = dw[t];
+    // dX = sum_t dY_t W_t^T: A = dY_t as [dk, N, B*H] (128-row boxes), B = W_t (128-row boxes)
+    ProjMaps mx;
+    std::memset(&mx, 0, sizeof mx);
+    CUresult r = CUDA_SUCCESS;
+    for (int t = 0; t < 3 && r == CUDA_SUCCESS; ++t) {
+        r = make_map(&mx.a[t], dy[t], B * H, N, d_k, 128);
+        if (r == CUDA_SUCCESS) r = make_map(&mx.b[t], w[t], 1, D, D, 128);
+    }
+    // dW_t = X^T dY_t: A = X as [D, N, B] (64-row boxes), B = dY_t (64-row boxes)
+    ProjMaps mw;
+    std::memset(&mw, 0, sizeof mw);
+    if (r == CUDA_SUCCESS) r = make_map(&mw.a[0], x, B, N, D, 64);
+    for (int t = 0; t < 3 && r == CUDA_SUCCESS; ++t) r = make_map(&mw.b[t], dy[t], B * H, N, d_k, 64);
+    if (r != CUDA_SUCCESS) return fail_driver("cuTensorMapEncodeTiled", r);
+    mw.a[1] = mw.a[2] = mw.a[0];
+    cudaError_t e = launch_proj_dx(mx, a, stream);
+    if (e == cudaSuccess) e = launch_proj_dw(mw, a, stream);
+    return e == cudaSuccess ? ATTN_OK : fail("attn_qkv_proj_bwd launch", e);
+}
+
 extern "C" attn_status vector_add(const float *a, const float *b, float *c, long long n,
                                   cudaStream_t stream)
 {

@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstdint>
+#include <cuda_bf16.h>
 
 namespace attn {
 
@@ -39,6 +40,21 @@ cudaError_t launch_bwd_convert(const BwdArgs &a, cudaStream_t stream);
 // The deterministic backward: preprocess (no accumulator), the main kernel without its dQ part,
 // then a query-stationary pass that computes dQ without atomics.
 cudaError_t launch_bwd_deterministic(const BwdArgs &a, cudaStream_t stream);
+// QKV projection (see proj.cu): tensor maps of the two operands (up to three each) and sizes.
+struct ProjMaps {
+    CUtensorMap a[3], b[3];
+};
+struct ProjArgs {
+    int B, N, D, H, dk;
+    __nv_bfloat16 *qkv[3];   // forward outputs Q, K, V [B,H,N,dk]
+    __nv_bfloat16 *dx;       // [B,N,D]
+    float *dw[3];            // [D,D] each
+    int *status;
+};
+cudaError_t launch_proj_fwd(const ProjMaps &m, const ProjArgs &a, cudaStream_t stream);
+cudaError_t launch_proj_dx(const ProjMaps &m, const ProjArgs &a, cudaStream_t stream);
+cudaError_t launch_proj_dw(const ProjMaps &m, const ProjArgs &a, cudaStream_t stream);
+
 cudaError_t launch_vector_add(const float *a, const float *b, float *c, long long n,
                               cudaStream_t stream);
 cudaError_t launch_wait_selftest(int *status, uint64_t limit_ns, cudaStream_t stream);

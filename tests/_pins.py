@@ -289,6 +289,57 @@ def pin_vector_add(lib):
     np.testing.assert_array_equal(oracle.vector_add(big, np.ones(3, np.float32), lib=lib), big)
 
 
+def pin_qkv_projection(lib):
+    """Section 1's Q = X W_Q (and K, V), head h = columns [h d_k, (h+1) d_k): W = I reproduces
+    the head-split X exactly; the map is linear in W; the backward satisfies
+    <dX, X> = sum_t <dW_t, W_t> (both equal sum_t <dY_t, Y_t>), matches central finite
+    differences, and matches torch autograd on the same fp64 inputs."""
+    import torch
+    rng = _rng(16)
+    B, N, D, H = 2, 5, 8, 2
+    d = D // H
+    x = _rand(rng, B, N, D)
+    ws = [_rand(rng, D, D) for _ in range(3)]
+    eye = np.eye(D)
+    q, k, v = oracle.qkv_proj(x, eye, eye, eye, H)
+    for h in range(H):
+        np.testing.assert_array_equal(q[:, h], x[:, :, h * d:(h + 1) * d])
+    w2 = _rand(rng, D, D)
+    lhs = oracle.qkv_proj(x, 2.5 * ws[0] + w2, ws[1], ws[2], H)[0]
+    rhs = 2.5 * oracle.qkv_proj(x, ws[0], ws[1], ws[2], H)[0] + oracle.qkv_proj(x, w2, ws[1], ws[2], H)[0]
+    np.testing.assert_allclose(lhs, rhs, rtol=0, atol=1e-12)
+    dys = [_rand(rng, B, H, N, d) for _ in range(3)]
+    dx, dwq, dwk, dwv = oracle.qkv_proj_bwd(x, *ws, *dys)
+    ys = oracle.qkv_proj(x, *ws, H)
+    L = sum(float((y * dy).sum()) for y, dy in zip(ys, dys))
+    np.testing.assert_allclose(float((dx * x).sum()), L, rtol=1e-12)
+    np.testing.assert_allclose(sum(float((dw * w).sum()) for dw, w in zip((dwq, dwk, dwv), ws)), L, rtol=1e-12)
+    # finite differences on a few entries of X and W_K
+    h_ = 1e-6
+
+    def loss(xx, wk):
+        yy = oracle.qkv_proj(xx, ws[0], wk, ws[2], H)
+        return sum(float((y * dy).sum()) for y, dy in zip(yy, dys))
+    for idx in ((0, 1, 3), (1, 4, 7)):
+        xp, xm = x.copy(), x.copy()
+        xp[idx] += h_
+        xm[idx] -= h_
+        np.testing.assert_allclose((loss(xp, ws[1]) - loss(xm, ws[1])) / (2 * h_), dx[idx], rtol=1e-6, atol=1e-8)
+    for idx in ((0, 0), (5, 2), (7, 6)):
+        wp, wm = ws[1].copy(), ws[1].copy()
+        wp[idx] += h_
+        wm[idx] -= h_
+        np.testing.assert_allclose((loss(x, wp) - loss(x, wm)) / (2 * h_), dwk[idx], rtol=1e-6, atol=1e-8)
+    # torch autograd
+    xt = torch.from_numpy(x.copy()).requires_grad_(True)
+    wt = [torch.from_numpy(w.copy()).requires_grad_(True) for w in ws]
+    out = [(xt @ w).reshape(B, N, H, d).permute(0, 2, 1, 3) for w in wt]
+    sum((o * torch.from_numpy(dy)).sum() for o, dy in zip(out, dys)).backward()
+    np.testing.assert_allclose(dx, xt.grad.numpy(), rtol=0, atol=1e-12)
+    for dw, w in zip((dwq, dwk, dwv), wt):
+        np.testing.assert_allclose(dw, w.grad.numpy(), rtol=0, atol=1e-12)
+
+
 ALL_PINS = [
     pin_rows_sum_to_one,
     pin_probabilities_match_library_softmax,
@@ -306,4 +357,5 @@ ALL_PINS = [
     pin_library_autograd,
     pin_rows_variants,
     pin_vector_add,
+    pin_qkv_projection,
 ]
