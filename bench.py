@@ -340,6 +340,30 @@ def run_ours(args, world, rank, local):
     probe_gbs = 12.0 * nvec / (p0.elapsed_time(p1) / 10 * 1e-3) / 1e9
     del va, vb, vc
 
+    # QKV projection (section 1: Q = X W_Q, ...) on the full ViT-B block shape, fwd and bwd
+    from self_attention_gb300.inputs import WORKLOADS as _W
+    bw = _W["vit_b_mhsa_block"]
+    PB, PN, PD, PH = bw.B, bw.N, bw.model_dim, bw.H
+    px = torch.randn(PB, PN, PD, device="cuda").bfloat16()
+    pw = [(torch.randn(PD, PD, device="cuda") / math.sqrt(PD)).bfloat16() for _ in range(3)]
+    pout = [torch.empty(PB, PH, PN, PD // PH, device="cuda", dtype=torch.bfloat16) for _ in range(3)]
+    pdy = [torch.randn(PB, PH, PN, PD // PH, device="cuda").bfloat16() for _ in range(3)]
+    pdx = torch.empty_like(px)
+    pdw = [torch.empty(PD, PD, device="cuda") for _ in range(3)]
+    proj = {}
+    for name, fn, fl in (
+            ("fwd", lambda: sa.attn_qkv_proj(px, *pw, *pout, PB, PN, PD, PH, PD // PH, stream), 6.0),
+            ("bwd", lambda: sa.attn_qkv_proj_bwd(px, *pw, *pdy, pdx, *pdw, PB, PN, PD, PH, PD // PH, stream), 12.0)):
+        for _ in range(3):
+            fn()
+        p0.record(stream)
+        for _ in range(20):
+            fn()
+        p1.record(stream)
+        torch.cuda.synchronize()
+        proj[name + "_tflops"] = fl * PB * PN * PD * PD / (p0.elapsed_time(p1) / 20 * 1e-3) / 1e12
+    del px, pw, pout, pdy, pdx, pdw
+
     res = reduce_over_ranks(local_res, world)
     if rank != 0:
         dist.destroy_process_group()
@@ -380,6 +404,8 @@ def run_ours(args, world, rank, local):
                      "note": f"peak = {peak_src} sustained dense bf16; achieved = 10*B*H*N^2*d "
                              "flops per launch / CUDA-event launch time"},
         "cpu_baseline": cpu,
+        "qkv_proj": {"workload": "vit_b_mhsa_block X [32, 576, 768] x 3 W [768, 768], 12 heads",
+                     **proj},
         "hbm_probe": {"kernel": "vector_add (fp32, 3 x 512 MiB)", "gbs": probe_gbs,
                       "frac_of_measured_copy": probe_gbs / peaks["hbm_gbs"]},
         "e2e": {"value": flops_total / (res["e2e_ms"] * 1e-3) / 1e12, "unit": UNIT,
