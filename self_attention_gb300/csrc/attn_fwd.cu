@@ -230,9 +230,10 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
             for (int u = 0; u < 8; ++u) mx[u] = __uint_as_float(r[u]);
 #pragma unroll
-            for (int i = 8; i < 128; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(r[i]));
-            const float smax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                     fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+            for (int i = 8; i < 128; i += 2)
+                mx[(i >> 1) & 7] = ptx::max3(mx[(i >> 1) & 7], __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+            const float smax = ptx::max3(ptx::max3(mx[0], mx[1], mx[2]), ptx::max3(mx[3], mx[4], mx[5]),
+                                         fmaxf(mx[6], mx[7]));
             const float mt = smax * scale_log2;
             float m_new = m, alpha = 1.f;
             bool rescale = false;
@@ -244,20 +245,29 @@ __global__ void __launch_bounds__(320, 1)
                 rescale = true;
             }
             const float neg_m = -m_new;
-            float sum[4] = {0.f, 0.f, 0.f, 0.f};
+            // x c - m for two scores per instruction (f32x2), 2^(.) on the MUFU, the row sum
+            // again two lanes at a time
+            const uint64_t c2 = ptx::f2_pack(scale_log2, scale_log2), nm2 = ptx::f2_pack(neg_m, neg_m);
+            uint64_t acc2[2] = {ptx::f2_pack(0.f, 0.f), ptx::f2_pack(0.f, 0.f)};
             // P = 2^(x - m) as bf16 pairs into TMEM over S_t, 32 keys (16 columns) at a time
 #pragma unroll
             for (int ch = 0; ch < 4; ++ch) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 32; i += 2) {
-                    const float p0 = ptx::ex2(fmaf(__uint_as_float(r[ch * 32 + i]), scale_log2, neg_m));
-                    const float p1 = ptx::ex2(fmaf(__uint_as_float(r[ch * 32 + i + 1]), scale_log2, neg_m));
-                    sum[(i >> 1) & 3] += p0 + p1;
+                    const uint64_t t = ptx::fma_f32x2(
+                        ptx::f2_pack(__uint_as_float(r[ch * 32 + i]), __uint_as_float(r[ch * 32 + i + 1])), c2, nm2);
+                    float t0, t1;
+                    ptx::f2_unpack(t, t0, t1);
+                    const float p0 = ptx::ex2(t0), p1 = ptx::ex2(t1);
+                    acc2[(i >> 1) & 1] = ptx::add_f32x2(acc2[(i >> 1) & 1], ptx::f2_pack(p0, p1));
                     pk[i >> 1] = ptx::pack_bf16x2(p0, p1);
                 }
                 ptx::tmem_st16(tS + ch * 16, pk);
             }
+            float sum[4];
+            ptx::f2_unpack(acc2[0], sum[0], sum[1]);
+            ptx::f2_unpack(acc2[1], sum[2], sum[3]);
             l = l * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
             m = m_new;
             if (rescale) {
