@@ -173,8 +173,8 @@ static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 namespace {
 
 // Workspace layout (every region 256-byte aligned), with N_pad = N rounded up to 64:
-//   D     [BH][N_pad] fp32   rowsum(dO o O); 0 in the padding
-//   LSE2  [BH][N_pad] fp32   lse * log2(e); +inf in the padding (probabilities there are 0)
+//   -D    [BH][N_pad] fp32   -rowsum(dO o O); 0 in the padding
+//   -LSE2 [BH][N_pad] fp32   -lse * log2(e); -inf in the padding (probabilities there are 0)
 //   dQacc [BH][N][d]  fp32   dQ accumulator (unscaled)
 struct WorkspaceLayout {
     size_t d_off, lse2_off, acc_off, total;

@@ -9,8 +9,8 @@
 //   dS = P o (dP - D),  dQ = scale * dS K,  dK = scale * dS^T Q.
 //
 // Three stream-ordered kernels:
-//   1. preprocess: D = rowsum(dO o O) and LSE2 = LSE log2 e (fp32, rows padded to a multiple
-//      of 64 with D = 0, LSE2 = +inf so that padded queries get zero probability), and zero
+//   1. preprocess: -D = -rowsum(dO o O) and -LSE2 = -LSE log2 e (fp32, rows padded to a
+//      multiple of 64 with 0 and -inf so that padded queries get zero probability), and zero
 //      the fp32 dQ accumulator.
 //   2. main: one CTA per 128-key tile j of one head, looping over all 64-row query tiles i.
 //        warp 12     TMA producer: K_j and V_j once; a ring of (Q_i, dO_i, LSE2_i, D_i).
@@ -57,8 +57,9 @@ struct BwdCfg {
 };
 
 // ------------------------------------------------------------------ 1. preprocess
-// Over the padded rows (bh, i), i < n_pad:  D = sum_c dO_ic O_ic and LSE2 = lse log2(e) for
-// i < n; D = 0 and LSE2 = +inf in the padding.  Then zero the dQ accumulator.
+// Over the padded rows (bh, i), i < n_pad, the negated statistics the later kernels add:
+// -D = -sum_c dO_ic O_ic and -LSE2 = -lse log2(e) for i < n; 0 and -inf in the padding (zero
+// probability there).  Then zero the dQ accumulator.
 template <int D>
 __global__ void __launch_bounds__(256)
     bwd_preprocess_kernel(const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restrict__ dout,
@@ -97,8 +98,8 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
         for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
         if (t < total && part == 0) {
-            dvec[prow] = acc;
-            lse2[prow] = i < n ? lse[row] * kLog2e : INFINITY;
+            dvec[prow] = -acc;
+            lse2[prow] = i < n ? -lse[row] * kLog2e : -INFINITY;
         }
     }
     if (!zero_acc) return;
@@ -323,7 +324,7 @@ __global__ void __launch_bounds__(448, 1)
         for (int it = wg; it < nq; it += 2) {
             const int b = wg, s = it % C::QST;
             const uint32_t ph = (it >> 1) & 1;
-            // this query tile's LSE2 (+inf past N) and D (0 past N), loaded with the tile
+            // this query tile's -LSE2 (-inf past N) and -D (0 past N), loaded with the tile
             const float *sl = sLD + s * 2 * C::BM;
             const float *sd = sl + C::BM;
             wait_bounded(&bar_sdp[b], ph, g);
@@ -347,22 +348,25 @@ __global__ void __launch_bounds__(448, 1)
                     ptx::tmem_ld16(tDP + (qt + 1) * 16, dpv[cur ^ 1]);
                 }
                 uint32_t pp[8], dsp[8];
+                const uint64_t c2 = ptx::f2_pack(scale_log2, scale_log2);
 #pragma unroll
-                for (int c = 0; c < 16; c += 4) {
-                    const float4 l4 = *reinterpret_cast<const float4 *>(sl + qt * 16 + c);
-                    const float4 d4 = *reinterpret_cast<const float4 *>(sd + qt * 16 + c);
-                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-                    float p[4], ds[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        p[e] = ptx::ex2(fmaf(__uint_as_float(sv[cur][c + e]), scale_log2, -lv[e]));
-                        if (!key_ok) p[e] = 0.f;
-                        ds[e] = p[e] * (__uint_as_float(dpv[cur][c + e]) - dv4[e]);
-                    }
-                    pp[c / 2] = ptx::pack_bf16x2(p[0], p[1]);
-                    pp[c / 2 + 1] = ptx::pack_bf16x2(p[2], p[3]);
-                    dsp[c / 2] = ptx::pack_bf16x2(ds[0], ds[1]);
-                    dsp[c / 2 + 1] = ptx::pack_bf16x2(ds[2], ds[3]);
+                for (int c = 0; c < 16; c += 2) {
+                    // nl = -LSE2 and nd = -D of queries c, c + 1 (two fp32 each, packed)
+                    const uint64_t nl = *reinterpret_cast<const uint64_t *>(sl + qt * 16 + c);
+                    const uint64_t nd = *reinterpret_cast<const uint64_t *>(sd + qt * 16 + c);
+                    const uint64_t x = ptx::fma_f32x2(
+                        ptx::f2_pack(__uint_as_float(sv[cur][c]), __uint_as_float(sv[cur][c + 1])), c2, nl);
+                    float x0, x1;
+                    ptx::f2_unpack(x, x0, x1);
+                    float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+                    if (!key_ok) p0 = p1 = 0.f;
+                    const uint64_t pq = ptx::f2_pack(p0, p1);
+                    const uint64_t dsq = ptx::mul_f32x2(
+                        pq, ptx::add_f32x2(ptx::f2_pack(__uint_as_float(dpv[cur][c]), __uint_as_float(dpv[cur][c + 1])), nd));
+                    float ds0, ds1;
+                    ptx::f2_unpack(dsq, ds0, ds1);
+                    pp[c / 2] = ptx::pack_bf16x2(p0, p1);
+                    dsp[c / 2] = ptx::pack_bf16x2(ds0, ds1);
                 }
                 ptx::tmem_st8(tS + qt * 8, pp);
 #pragma unroll
@@ -632,8 +636,8 @@ __global__ void __launch_bounds__(320, 1)
         const bool row_ok = row < n;
         const uint32_t lane_off = (uint32_t)(cw * 32) << 16;
         const float scale_log2 = scale * kLog2e;
-        const float l2 = row_ok ? lse2[(size_t)bh * n_pad + row] : INFINITY;
-        const float dr = row_ok ? dvec[(size_t)bh * n_pad + row] : 0.f;
+        const float nl2 = row_ok ? lse2[(size_t)bh * n_pad + row] : -INFINITY;   // -LSE2
+        const float nd = row_ok ? dvec[(size_t)bh * n_pad + row] : 0.f;          // -D
         for (int j = wg; j < nk; j += 2) {
             const int b = wg;
             wait_bounded(&bar_sdp[b], (j >> 1) & 1, g);
@@ -657,12 +661,12 @@ __global__ void __launch_bounds__(320, 1)
                 uint32_t dsp[8];
 #pragma unroll
                 for (int c = 0; c < 16; c += 2) {
-                    float p0 = ptx::ex2(fmaf(__uint_as_float(sv[cur][c]), scale_log2, -l2));
-                    float p1 = ptx::ex2(fmaf(__uint_as_float(sv[cur][c + 1]), scale_log2, -l2));
+                    float p0 = ptx::ex2(fmaf(__uint_as_float(sv[cur][c]), scale_log2, nl2));
+                    float p1 = ptx::ex2(fmaf(__uint_as_float(sv[cur][c + 1]), scale_log2, nl2));
                     if (qt * 16 + c >= valid) p0 = 0.f;
                     if (qt * 16 + c + 1 >= valid) p1 = 0.f;
-                    dsp[c / 2] = ptx::pack_bf16x2(p0 * (__uint_as_float(dpv[cur][c]) - dr),
-                                                  p1 * (__uint_as_float(dpv[cur][c + 1]) - dr));
+                    dsp[c / 2] = ptx::pack_bf16x2(p0 * (__uint_as_float(dpv[cur][c]) + nd),
+                                                  p1 * (__uint_as_float(dpv[cur][c + 1]) + nd));
                 }
                 ptx::tmem_st8(tS + qt * 8, dsp);
                 if (qt < 3) {

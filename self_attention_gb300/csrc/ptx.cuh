@@ -355,6 +355,13 @@ __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b)
     return d;
 }
 
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 // max(a, b, c) in one instruction.
 __device__ __forceinline__ float max3(float a, float b, float c)
 {
