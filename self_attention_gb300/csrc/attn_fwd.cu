@@ -10,7 +10,9 @@
 // per-row statistic the backward pass needs ("Recomputation in backpropagation") is stored
 // as LSE = log sum_j exp(scale * q_i . k_j).
 //
-// Blackwell mapping (one CTA = 256 query rows of one head, two tiles of 128):
+// Blackwell mapping of fwd_kernel<D, NQ> (one CTA = NQ query tiles of 128 rows of one head;
+// NQ = 2 for d = 128, shown here; NQ = 1 for d = 64, where the softmax ALU work per tile equals
+// the matrix work and two one-tile CTAs per SM overlap better than two tiles in one CTA):
 //   warp 8      TMA producer: Q tiles once, then a ring of K and V tiles (128 keys each).
 //   warp 9      tcgen05 issuer: S_t = Q_t K_j^T into TMEM (fp32), then O_t += P_t V_j with
 //               P_t read from TMEM (bf16, written over S_t) and V_j from shared memory.
@@ -21,6 +23,8 @@
 //               division uses the same m).  The two tiles alternate on the tensor core, so
 //               one tile's softmax overlaps the other tile's matrix products.
 // TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+d), O_1 [256+d,256+2d).
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -32,27 +36,35 @@ constexpr float kLn2 = 0.6931471805599453f;
 // The running maximum is only moved (and O rescaled) when a tile raises it by more than this
 // many powers of two; in between, probabilities may reach 2^kTau, far from fp32/bf16 limits.
 constexpr float kTau = 8.0f;
+// d = 64 runs one 128-row query tile per CTA, two CTAs per SM; up to this sequence length
+// the CTAs are persistent (the per-item latencies dominate there), beyond it one CTA per tile.
+constexpr int kFwdPersistentMaxN = 2048;
 
-template <int D>
+template <int D, int NQ_>
 struct FwdCfg {
     static constexpr int BM = 128;  // query rows per tile (= TMEM lanes)
-    static constexpr int NQ = 2;    // query tiles per CTA
+    static constexpr int NQ = NQ_;  // query tiles per CTA
     static constexpr int BN = 128;  // keys per K/V tile
-    static constexpr int STAGES = (D == 64) ? 4 : 2;
+    // One tile per CTA (short sequences) keeps shared memory and TMEM small enough for two
+    // CTAs per SM, which then hide each other's load and epilogue latency.
+    static constexpr int STAGES = NQ == 1 ? 2 : (D == 64) ? 4 : 2;
     static constexpr int Q_BYTES = BM * D * 2;
     static constexpr int KV_BYTES = BN * D * 2;
     static constexpr int SMEM_BYTES = NQ * Q_BYTES + 2 * STAGES * KV_BYTES + 1024;
-    static constexpr int THREADS = 320;
-    static constexpr uint32_t TM_O = 256;  // first O column
+    static constexpr int TMA_WARP = 4 * NQ, MMA_WARP = 4 * NQ + 1;
+    static constexpr int THREADS = 32 * (4 * NQ + 2);
+    static constexpr uint32_t TM_O = NQ * 128;  // first O column
+    static constexpr uint32_t TM_COLS = NQ == 1 ? 256 : 512;
+    static constexpr int MIN_BLOCKS = NQ == 1 ? 2 : 1;
 };
 
-template <int D>
-__global__ void __launch_bounds__(320, 1)
+template <int D, int NQ>
+__global__ void __launch_bounds__(FwdCfg<D, NQ>::THREADS, FwdCfg<D, NQ>::MIN_BLOCKS)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16 *__restrict__ o,
                float *__restrict__ lse, int n, int n_qblocks, float scale_log2, int *status)
 {
-    using C = FwdCfg<D>;
+    using C = FwdCfg<D, NQ>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
     uint8_t *sQ = smem;
@@ -80,7 +92,7 @@ __global__ void __launch_bounds__(320, 1)
             ptx::mbar_init(&bar_vf[s], 1);
             ptx::mbar_init(&bar_ve[s], 1);
         }
-        for (int t = 0; t < 2; ++t) {
+        for (int t = 0; t < C::NQ; ++t) {
             ptx::mbar_init(&bar_s[t], 1);
             ptx::mbar_init(&bar_p[t], 128);
             ptx::mbar_init(&bar_o[t], 1);
@@ -88,8 +100,8 @@ __global__ void __launch_bounds__(320, 1)
         ptx::mbar_init(&bar_done, 1);
         ptx::fence_mbar_init();
     }
-    if (warp == 9) {
-        ptx::tmem_alloc(&tmem_sh, 512);
+    if (warp == C::MMA_WARP) {
+        ptx::tmem_alloc(&tmem_sh, C::TM_COLS);
         ptx::tmem_relinquish();
     }
     ptx::tc_fence_before();
@@ -97,7 +109,7 @@ __global__ void __launch_bounds__(320, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = tmem_sh;
 
-    if (warp == 8) {
+    if (warp == C::TMA_WARP) {
         // ---------------------------------------------------------------- TMA producer
         if (ptx::elect_one()) {
             ptx::tma_prefetch_desc(&tm_q);
@@ -130,7 +142,7 @@ __global__ void __launch_bounds__(320, 1)
                 wait_bounded(&bar_vf[s], ph, g);
             }
         }
-    } else if (warp == 9) {
+    } else if (warp == C::MMA_WARP) {
         // ---------------------------------------------------------------- MMA issuer
         if (ptx::elect_one()) {
             const uint32_t idS = ptx::idesc_bf16_f32(128, C::BN, false, false);
@@ -160,11 +172,16 @@ __global__ void __launch_bounds__(320, 1)
             wait_bounded(&bar_q, 0, g);
             wait_bounded(&bar_kf[0], 0, g);
             ptx::tc_fence_after();
-            issue_s(0, 0);
-            ptx::mma_commit(&bar_s[0]);
-            issue_s(1, 0);
-            ptx::mma_commit(&bar_s[1]);
+#pragma unroll
+            for (int t = 0; t < C::NQ; ++t) {
+                issue_s(t, 0);
+                ptx::mma_commit(&bar_s[t]);
+            }
             ptx::mma_commit(&bar_ke[0]);
+            // Per key tile j and query tile t: O_t += P_t V_j as soon as P_t is in TMEM, then
+            // S_t of tile j + 1 into the same columns (the MMAs run in issue order, so P_t has
+            // been read by then).  With two query tiles, one tile's products overlap the
+            // other tile's softmax.
             for (int j = 0; j < nkv; ++j) {
                 const int s = j % C::STAGES;
                 const uint32_t ph = (j / C::STAGES) & 1;
@@ -172,27 +189,23 @@ __global__ void __launch_bounds__(320, 1)
                 const int sn = jn % C::STAGES;
                 const uint32_t phn = (jn / C::STAGES) & 1;
                 wait_bounded(&bar_vf[s], ph, g);
-                wait_bounded(&bar_p[0], j & 1, g);
-                ptx::tc_fence_after();
-                issue_pv(0, s, j > 0);
-                if (jn < nkv) {
-                    wait_bounded(&bar_kf[sn], phn, g);
+#pragma unroll
+                for (int t = 0; t < C::NQ; ++t) {
+                    wait_bounded(&bar_p[t], j & 1, g);
                     ptx::tc_fence_after();
-                    issue_s(0, sn);
-                    ptx::mma_commit(&bar_s[0]);
-                } else {
-                    ptx::mma_commit(&bar_o[0]);
-                }
-                wait_bounded(&bar_p[1], j & 1, g);
-                ptx::tc_fence_after();
-                issue_pv(1, s, j > 0);
-                ptx::mma_commit(&bar_ve[s]);
-                if (jn < nkv) {
-                    issue_s(1, sn);
-                    ptx::mma_commit(&bar_s[1]);
-                    ptx::mma_commit(&bar_ke[sn]);
-                } else {
-                    ptx::mma_commit(&bar_o[1]);
+                    issue_pv(t, s, j > 0);
+                    if (t == C::NQ - 1) ptx::mma_commit(&bar_ve[s]);
+                    if (jn < nkv) {
+                        if (t == 0) {
+                            wait_bounded(&bar_kf[sn], phn, g);
+                            ptx::tc_fence_after();
+                        }
+                        issue_s(t, sn);
+                        ptx::mma_commit(&bar_s[t]);
+                        if (t == C::NQ - 1) ptx::mma_commit(&bar_ke[sn]);
+                    } else {
+                        ptx::mma_commit(&bar_o[t]);
+                    }
                 }
             }
             // Every MMA must have finished before TMEM is released (matters after a timeout).
@@ -315,23 +328,350 @@ __global__ void __launch_bounds__(320, 1)
 
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == C::MMA_WARP) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem, 512);
+        ptx::tmem_dealloc(tmem, C::TM_COLS);
     }
 }
 
+// Persistent variant for d = 64: one query tile per work item, items (head, 128-row block)
+// taken in a grid-stride order by CTAs that stay resident (two per SM), so the loads of the
+// next item, the tail of the previous one and the other CTA's work hide each other's latency.
+//   warp 4      TMA: Q of each item into one of two Q buffers, K/V tiles through one ring that
+//               runs across items.
+//   warp 5      tcgen05: S = Q K_j^T, O_b += P V_j (b = item parity: two O accumulators, so
+//               an item's products start while the previous item's O is still being written
+//               out); the next S, of this item or the next, follows each P V at once.
+//   warps 0-3   softmax as above, then the epilogue of the item from O_b.
+// TMEM columns: S [0,128), O_0 [128,128+d), O_1 [128+d,128+2d).
 template <int D>
+struct PersistCfg {
+    static constexpr int BM = 128, BN = 128;
+    static constexpr int STAGES = 2;
+    static constexpr int Q_BYTES = BM * D * 2;
+    static constexpr int KV_BYTES = BN * D * 2;
+    static constexpr int SMEM_BYTES = 2 * Q_BYTES + 2 * STAGES * KV_BYTES + 1024;
+    static constexpr int THREADS = 192;
+    static constexpr int TMA_WARP = 4, MMA_WARP = 5;
+    static constexpr uint32_t TM_O = 128;
+    static constexpr uint32_t TM_COLS = 128 + 2 * D <= 256 ? 256 : 512;
+};
+
+template <int D>
+__global__ void __launch_bounds__(192, 2)
+    fwd_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16 *__restrict__ o,
+                          float *__restrict__ lse, int n, int n_qblocks, int n_items,
+                          float scale_log2, int *status)
+{
+    using C = PersistCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    uint8_t *sQ = smem;                         // two Q buffers
+    uint8_t *sK = sQ + 2 * C::Q_BYTES;
+    uint8_t *sV = sK + C::STAGES * C::KV_BYTES;
+
+    __shared__ uint64_t bar_qf[2], bar_qe[2];
+    __shared__ uint64_t bar_kf[C::STAGES], bar_ke[C::STAGES], bar_vf[C::STAGES], bar_ve[C::STAGES];
+    __shared__ uint64_t bar_s, bar_p, bar_of[2], bar_oe[2], bar_done;
+    __shared__ uint32_t tmem_sh;
+    __shared__ int abort_sh;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nkv = (n + C::BN - 1) / C::BN;
+    const Guard g{&abort_sh, status, kWaitLimitNs};
+    const int first = blockIdx.x, stride = gridDim.x;
+
+    if (threadIdx.x == 0) {
+        abort_sh = 0;
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(&bar_qf[b], 1);
+            ptx::mbar_init(&bar_qe[b], 1);
+            ptx::mbar_init(&bar_of[b], 1);
+            ptx::mbar_init(&bar_oe[b], 128);
+        }
+        for (int s = 0; s < C::STAGES; ++s) {
+            ptx::mbar_init(&bar_kf[s], 1);
+            ptx::mbar_init(&bar_ke[s], 1);
+            ptx::mbar_init(&bar_vf[s], 1);
+            ptx::mbar_init(&bar_ve[s], 1);
+        }
+        ptx::mbar_init(&bar_s, 1);
+        ptx::mbar_init(&bar_p, 128);
+        ptx::mbar_init(&bar_done, 1);
+        ptx::fence_mbar_init();
+    }
+    if (warp == C::MMA_WARP) {
+        ptx::tmem_alloc(&tmem_sh, C::TM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = tmem_sh;
+
+    if (warp == C::TMA_WARP) {
+        // ---------------------------------------------------------------- TMA producer
+        if (ptx::elect_one()) {
+            ptx::tma_prefetch_desc(&tm_q);
+            ptx::tma_prefetch_desc(&tm_k);
+            ptx::tma_prefetch_desc(&tm_v);
+            int kt = 0;   // K/V tiles loaded so far (ring position)
+            int li = 0;
+            for (int item = first; item < n_items; item += stride, ++li) {
+                const int bh = item / n_qblocks, q0 = (item % n_qblocks) * C::BM;
+                const int qb = li & 1;
+                wait_bounded(&bar_qe[qb], ((li >> 1) & 1) ^ 1, g);
+                ptx::mbar_arrive_expect_tx(&bar_qf[qb], C::Q_BYTES);
+                for (int h = 0; h < D / 64; ++h)
+                    ptx::tma_load_3d(sQ + qb * C::Q_BYTES + h * C::BM * 128, &tm_q, &bar_qf[qb],
+                                     h * 64, q0, bh);
+                for (int j = 0; j < nkv; ++j, ++kt) {
+                    const int s = kt % C::STAGES;
+                    const uint32_t ph = (kt / C::STAGES) & 1;
+                    wait_bounded(&bar_ke[s], ph ^ 1, g);
+                    ptx::mbar_arrive_expect_tx(&bar_kf[s], C::KV_BYTES);
+                    for (int h = 0; h < D / 64; ++h)
+                        ptx::tma_load_3d(sK + s * C::KV_BYTES + h * C::BN * 128, &tm_k, &bar_kf[s],
+                                         h * 64, j * C::BN, bh);
+                    wait_bounded(&bar_ve[s], ph ^ 1, g);
+                    ptx::mbar_arrive_expect_tx(&bar_vf[s], C::KV_BYTES);
+                    for (int h = 0; h < D / 64; ++h)
+                        ptx::tma_load_3d(sV + s * C::KV_BYTES + h * C::BN * 128, &tm_v, &bar_vf[s],
+                                         h * 64, j * C::BN, bh);
+                }
+            }
+            // Do not leave the CTA with copies in flight (matters only after a timeout).
+            for (int t = (kt > C::STAGES ? kt - C::STAGES : 0); t < kt; ++t) {
+                wait_bounded(&bar_kf[t % C::STAGES], (t / C::STAGES) & 1, g);
+                wait_bounded(&bar_vf[t % C::STAGES], (t / C::STAGES) & 1, g);
+            }
+        }
+    } else if (warp == C::MMA_WARP) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (ptx::elect_one()) {
+            const uint32_t idS = ptx::idesc_bf16_f32(128, C::BN, false, false);
+            const uint32_t idO = ptx::idesc_bf16_f32(128, D, false, true);
+            const uint32_t q_base = ptx::smem_u32(sQ), k_base = ptx::smem_u32(sK),
+                           v_base = ptx::smem_u32(sV);
+            auto issue_s = [&](int qb, int s) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * (C::BM * 128) + (kk & 3) * 32;
+                    const uint64_t a = ptx::sdesc_sw128(q_base + qb * C::Q_BYTES + off, 16, 1024);
+                    const uint64_t b = ptx::sdesc_sw128(k_base + s * C::KV_BYTES + off, 16, 1024);
+                    ptx::mma_ss(tmem, a, b, idS, kk > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_pv = [&](int ob, int s, bool acc) {
+#pragma unroll
+                for (int kk = 0; kk < C::BN / 16; ++kk) {
+                    const uint64_t b =
+                        ptx::sdesc_sw128(v_base + s * C::KV_BYTES + kk * 2048, C::BN * 128, 1024);
+                    ptx::mma_ts(tmem + C::TM_O + ob * D, tmem + kk * 8, b, idO,
+                                (acc || kk > 0) ? 1u : 0u);
+                }
+            };
+            // S of global step kt (item li, key tile j); Q_li is free once its last S is done.
+            auto next_s = [&](int li, int j, int kt) {
+                const int s = kt % C::STAGES;
+                wait_bounded(&bar_kf[s], (kt / C::STAGES) & 1, g);
+                if (j == 0) wait_bounded(&bar_qf[li & 1], (li >> 1) & 1, g);
+                ptx::tc_fence_after();
+                issue_s(li & 1, s);
+                ptx::mma_commit(&bar_s);
+                ptx::mma_commit(&bar_ke[s]);
+                if (j == nkv - 1) ptx::mma_commit(&bar_qe[li & 1]);
+            };
+            if (first < n_items) next_s(0, 0, 0);
+            int kt = 0, li = 0;
+            for (int item = first; item < n_items; item += stride, ++li) {
+                const int ob = li & 1;
+                for (int j = 0; j < nkv; ++j, ++kt) {
+                    const int s = kt % C::STAGES;
+                    wait_bounded(&bar_vf[s], (kt / C::STAGES) & 1, g);
+                    if (j == 0) wait_bounded(&bar_oe[ob], ((li >> 1) & 1) ^ 1, g);  // O_b written out
+                    wait_bounded(&bar_p, kt & 1, g);
+                    ptx::tc_fence_after();
+                    issue_pv(ob, s, j > 0);
+                    ptx::mma_commit(&bar_ve[s]);
+                    if (j == nkv - 1) ptx::mma_commit(&bar_of[ob]);
+                    if (j + 1 < nkv)
+                        next_s(li, j + 1, kt + 1);
+                    else if (item + stride < n_items)
+                        next_s(li + 1, 0, kt + 1);
+                }
+            }
+            // Every MMA must have finished before TMEM is released (matters after a timeout).
+            ptx::mma_commit(&bar_done);
+            wait_bounded(&bar_done, 0, g);
+        }
+    } else {
+        // ---------------------------------------------------------------- softmax warpgroup
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const uint32_t tS = tmem + lane_off;
+        int kt = 0, li = 0;
+        for (int item = first; item < n_items; item += stride, ++li) {
+            const int bh = item / n_qblocks;
+            const int row = (item % n_qblocks) * C::BM + warp * 32 + lane;
+            const int ob = li & 1;
+            const uint32_t tO = tmem + lane_off + C::TM_O + ob * D;
+            float m = -INFINITY, l = 0.f;
+            for (int j = 0; j < nkv; ++j, ++kt) {
+                wait_bounded(&bar_s, kt & 1, g);
+                ptx::tc_fence_after();
+                uint32_t r[128];
+                ptx::tmem_ld32_at<0>(tS + 0, r);
+                ptx::tmem_ld32_at<32>(tS + 32, r);
+                ptx::tmem_ld32_at<64>(tS + 64, r);
+                ptx::tmem_ld32_at<96>(tS + 96, r);
+                ptx::tmem_ld_wait();
+                reg_fence(r);
+                const int valid = n - j * C::BN;
+                if (valid < C::BN) {
+#pragma unroll
+                    for (int i = 0; i < 128; ++i)
+                        if (i >= valid) r[i] = __float_as_uint(-INFINITY);
+                }
+                float mx[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) mx[u] = __uint_as_float(r[u]);
+#pragma unroll
+                for (int i = 8; i < 128; i += 2)
+                    mx[(i >> 1) & 7] = ptx::max3(mx[(i >> 1) & 7], __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+                const float smax = ptx::max3(ptx::max3(mx[0], mx[1], mx[2]), ptx::max3(mx[3], mx[4], mx[5]),
+                                             fmaxf(mx[6], mx[7]));
+                const float mt = smax * scale_log2;
+                float m_new = m, alpha = 1.f;
+                bool rescale = false;
+                if (j == 0) {
+                    m_new = mt;
+                } else if (__any_sync(0xffffffffu, mt > m + kTau)) {
+                    m_new = fmaxf(m, mt);
+                    alpha = ptx::ex2(m - m_new);
+                    rescale = true;
+                }
+                const float neg_m = -m_new;
+                const uint64_t c2 = ptx::f2_pack(scale_log2, scale_log2), nm2 = ptx::f2_pack(neg_m, neg_m);
+                uint64_t acc2[2] = {ptx::f2_pack(0.f, 0.f), ptx::f2_pack(0.f, 0.f)};
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        const uint64_t t = ptx::fma_f32x2(
+                            ptx::f2_pack(__uint_as_float(r[ch * 32 + i]), __uint_as_float(r[ch * 32 + i + 1])), c2, nm2);
+                        float t0, t1;
+                        ptx::f2_unpack(t, t0, t1);
+                        const float p0 = ptx::ex2(t0), p1 = ptx::ex2(t1);
+                        acc2[(i >> 1) & 1] = ptx::add_f32x2(acc2[(i >> 1) & 1], ptx::f2_pack(p0, p1));
+                        pk[i >> 1] = ptx::pack_bf16x2(p0, p1);
+                    }
+                    ptx::tmem_st16(tS + ch * 16, pk);
+                }
+                float sum[4];
+                ptx::f2_unpack(acc2[0], sum[0], sum[1]);
+                ptx::f2_unpack(acc2[1], sum[2], sum[3]);
+                l = l * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
+                m = m_new;
+                if (rescale) {
+                    // O_b holds this item's partial sums up to key tile j - 1 (its P V for
+                    // tile j is issued only after this arrival).
+#pragma unroll
+                    for (int c = 0; c < D; c += 32) {
+                        uint32_t ov[32];
+                        ptx::tmem_ld32(tO + c, ov);
+                        ptx::tmem_ld_wait();
+                        reg_fence(ov);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                        ptx::tmem_st32(tO + c, ov);
+                    }
+                }
+                ptx::tmem_st_wait();
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(&bar_p);
+            }
+
+            // epilogue of this item: O = O_b / l (bf16), LSE = (m + log2 l) ln 2
+            wait_bounded(&bar_of[ob], (li >> 1) & 1, g);
+            ptx::tc_fence_after();
+            const float inv_l = 1.f / l;
+            __nv_bfloat16 *orow = o + ((size_t)bh * n + (row < n ? row : 0)) * D;
+#pragma unroll
+            for (int c = 0; c < D; c += 32) {
+                uint32_t ov[32];
+                ptx::tmem_ld32(tO + c, ov);
+                ptx::tmem_ld_wait();
+                reg_fence(ov);
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    pk[i] = ptx::pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l,
+                                             __uint_as_float(ov[2 * i + 1]) * inv_l);
+                if (row < n) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c);
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4)
+                        dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                }
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&bar_oe[ob]);
+            if (row < n) lse[(size_t)bh * n + row] = (m + log2f(l)) * kLn2;
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == C::MMA_WARP) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, C::TM_COLS);
+    }
+}
+
+int sm_count()
+{
+    static int cached[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return 148;
+    if (cached[dev] == 0) {
+        int sms = 0;
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cached[dev] = sms > 0 ? sms : 148;
+    }
+    return cached[dev];
+}
+
+template <int D>
+cudaError_t launch_fwd_persistent(const FwdArgs &a, cudaStream_t stream)
+{
+    using C = PersistCfg<D>;
+    cudaError_t e = cudaFuncSetAttribute(fwd_persistent_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int n_qblocks = (a.n + C::BM - 1) / C::BM;
+    const long long items = (long long)n_qblocks * a.bh;
+    // Two CTAs per SM: TMEM (256 columns each), shared memory and registers are sized for it.
+    const long long ctas = std::min<long long>(items, 2LL * sm_count());
+    fwd_persistent_kernel<D><<<(unsigned)ctas, C::THREADS, C::SMEM_BYTES, stream>>>(
+        a.tm_q, a.tm_k, a.tm_v, reinterpret_cast<__nv_bfloat16 *>(a.o), a.lse, a.n, n_qblocks,
+        (int)items, a.scale * kLog2e, a.status);
+    return cudaGetLastError();
+}
+
+template <int D, int NQ>
 cudaError_t launch_fwd_d(const FwdArgs &a, cudaStream_t stream)
 {
-    using C = FwdCfg<D>;
-    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM_BYTES);
+    using C = FwdCfg<D, NQ>;
+    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, NQ>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int rows_per_cta = C::NQ * C::BM;
     const int n_qblocks = (a.n + rows_per_cta - 1) / rows_per_cta;
     const long long ctas = (long long)n_qblocks * a.bh;
-    fwd_kernel<D><<<(unsigned)ctas, C::THREADS, C::SMEM_BYTES, stream>>>(
+    fwd_kernel<D, NQ><<<(unsigned)ctas, C::THREADS, C::SMEM_BYTES, stream>>>(
         a.tm_q, a.tm_k, a.tm_v, reinterpret_cast<__nv_bfloat16 *>(a.o), a.lse, a.n, n_qblocks,
         a.scale * kLog2e, a.status);
     return cudaGetLastError();
@@ -341,7 +681,9 @@ cudaError_t launch_fwd_d(const FwdArgs &a, cudaStream_t stream)
 
 cudaError_t launch_fwd(const FwdArgs &a, cudaStream_t stream)
 {
-    return a.d == 64 ? launch_fwd_d<64>(a, stream) : launch_fwd_d<128>(a, stream);
+    if (a.d == 128) return launch_fwd_d<128, 2>(a, stream);
+    if (a.n <= kFwdPersistentMaxN) return launch_fwd_persistent<64>(a, stream);
+    return launch_fwd_d<64, 1>(a, stream);
 }
 
 }  // namespace attn
