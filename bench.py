@@ -57,6 +57,8 @@ def parse_args(argv=None):
     p.add_argument("--cpu-baseline-tokens", type=int, default=8192,
                    help="tokens of one head the CPU oracle runs on for cpu_baseline (~10-30 s)")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the per-workload forward/backward table")
     return p.parse_args(argv)
 
 
@@ -220,6 +222,74 @@ def run_reference(args, world, rank):
     return 0
 
 
+def time_configs(sa, stream, peaks):
+    """Forward and backward (all three phases) of every workload, attention only, on device
+    inputs of the workload's shape and distribution.  Warm: back-to-back launches, mean.
+    Flushed (the small shapes, whose inputs fit in L2): a 256 MB buffer is written before each
+    launch, outside its events; median.  GB/s counts the algorithmic bytes: forward reads Q, K,
+    V and writes O, LSE; backward reads Q, K, V, O, dO, LSE and writes dQ, dK, dV."""
+    import torch
+    from self_attention_gb300.inputs import WORKLOADS
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    out = {}
+    for name, w in WORKLOADS.items():
+        B, H, N, D = w.B, w.H, w.N, w.d
+        q = (torch.randn(B, H, N, D, device="cuda") * w.qk_std).bfloat16()
+        k = (torch.randn(B, H, N, D, device="cuda") * w.qk_std).bfloat16()
+        v, do = torch.randn_like(q), torch.randn_like(q)
+        o, dq, dk, dv = (torch.empty_like(q) for _ in range(4))
+        lse = torch.empty(B, H, N, device="cuda")
+        wsb = sa.attn_bwd_workspace_size(B, H, N, D)
+        ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+        fwd = lambda: sa.attn_fwd(q, k, v, o, lse, B, H, N, D, w.scale, stream)
+        bwd = lambda: sa.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, wsb, B, H, N, D, w.scale,
+                                  stream)
+        flops = B * H * N * N * D
+        small = 2 * 4 * B * H * N * D < 130e6   # forward inputs + outputs fit in the 129 MB L2
+        rep = 200 if small else (20 if flops < 1e11 else 5)
+        row = {"B": B, "H": H, "N": N, "d_k": D}
+        for tag, fn, fl, nbytes in (
+                ("fwd", fwd, 4 * flops, B * H * N * D * 2 * 4 + 4 * B * H * N),
+                ("bwd", bwd, 10 * flops, B * H * N * D * 2 * 8 + 4 * B * H * N)):
+            for _ in range(5):
+                fn()
+            a, b = ev(), ev()
+            a.record(stream)
+            for _ in range(rep):
+                fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            us = a.elapsed_time(b) / rep * 1e3
+            row[tag + "_us"] = us
+            row[tag + "_tflops"] = fl / us / 1e6
+            row[tag + "_gbs"] = nbytes / us / 1e3
+            if small:
+                ts = []
+                for _ in range(30):
+                    flush.fill_(1)
+                    a, b = ev(), ev()
+                    a.record(stream)
+                    fn()
+                    b.record(stream)
+                    b.synchronize()
+                    ts.append(a.elapsed_time(b) * 1e3)
+                us_f = statistics.median(ts)
+                row[tag + "_us_flushed"] = us_f
+                row[tag + "_gbs_flushed"] = nbytes / us_f / 1e3
+                row[tag + "_frac_of_hbm_flushed"] = row[tag + "_gbs_flushed"] / peaks["hbm_gbs"]
+            row[tag + "_frac_of_hbm"] = row[tag + "_gbs"] / peaks["hbm_gbs"]
+            row[tag + "_frac_of_bf16_peak"] = row[tag + "_tflops"] / peaks["bf16_tflops"]
+        if sa.attn_get_device_status() != 0:
+            raise RuntimeError(f"device status reported a kernel timeout on {name}")
+        out[name] = row
+        del q, k, v, do, o, dq, dk, dv, lse, ws
+    del flush
+    torch.cuda.synchronize()
+    return out
+
+
 def run_ours(args, world, rank, local):
     import torch
     import torch.distributed as dist
@@ -364,6 +434,10 @@ def run_ours(args, world, rank, local):
         proj[name + "_tflops"] = fl * PB * PN * PD * PD / (p0.elapsed_time(p1) / 20 * 1e-3) / 1e12
     del px, pw, pout, pdy, pdx, pdw
 
+    configs = None
+    if world == 1 and not args.no_configs:
+        configs = time_configs(sa, stream, load_peaks()[0])
+
     res = reduce_over_ranks(local_res, world)
     if rank != 0:
         dist.destroy_process_group()
@@ -406,6 +480,7 @@ def run_ours(args, world, rank, local):
         "cpu_baseline": cpu,
         "qkv_proj": {"workload": "vit_b_mhsa_block X [32, 576, 768] x 3 W [768, 768], 12 heads",
                      **proj},
+        "configs": configs,
         "hbm_probe": {"kernel": "vector_add (fp32, 3 x 512 MiB)", "gbs": probe_gbs,
                       "frac_of_measured_copy": probe_gbs / peaks["hbm_gbs"]},
         "e2e": {"value": flops_total / (res["e2e_ms"] * 1e-3) / 1e12, "unit": UNIT,

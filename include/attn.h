@@ -63,10 +63,10 @@ attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float
                      int H, int N, int d_k, float scale, cudaStream_t stream);
 
 /*
- * Bytes of device workspace attn_bwd() needs for these sizes: two per-row fp32 vectors
- * (-rowsum(dO o O) and -lse * log2(e), [B,H] x N rounded up to 64) and an fp32 dQ
- * accumulator ([B,H,N,d_k]), each region 256-byte aligned.  Returns 0 if the sizes are
- * unsupported.
+ * Bytes of device workspace attn_bwd() needs for these sizes: two fp32 statistics per row
+ * (-lse * log2(e) and -rowsum(dO o O), [B,H] x N rounded up to 128, stored interleaved per
+ * pair of rows) and an fp32 dQ accumulator ([B,H,N,d_k]), each region 256-byte aligned.
+ * Returns 0 if the sizes are unsupported.
  */
 size_t attn_bwd_workspace_size(int B, int H, int N, int d_k);
 
@@ -109,7 +109,7 @@ attn_status attn_bwd_deterministic(const void *q, const void *k, const void *v, 
  * they produce exactly what attn_bwd() produces.
  *
  * attn_bwd_preprocess: reads o, dout and lse; writes into the workspace -D_i, with
- *   D_i = sum_c dO_ic O_ic, and -lse_i * log2(e) (rows padded to a multiple of 64; padding rows
+ *   D_i = sum_c dO_ic O_ic, and -lse_i * log2(e) (rows padded to a multiple of 128; padding rows
  *   get 0 and -inf, i.e. zero probability), and zeroes the workspace's fp32 dQ accumulator.
  * attn_bwd_main: for every 128-key tile, recomputes P = 2^(scale log2(e) q.k - lse log2(e))
  *   from q, k and the workspace, writes dk (= scale * dS^T Q) and dv (= P^T dO), and adds

@@ -172,21 +172,21 @@ static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 namespace {
 
-// Workspace layout (every region 256-byte aligned), with N_pad = N rounded up to 64:
-//   -D    [BH][N_pad] fp32   -rowsum(dO o O); 0 in the padding
-//   -LSE2 [BH][N_pad] fp32   -lse * log2(e); -inf in the padding (probabilities there are 0)
-//   dQacc [BH][N][d]  fp32   dQ accumulator (unscaled)
+// Workspace layout (every region 256-byte aligned), with N_pad = N rounded up to 128:
+//   stats [BH][N_pad / 2][4] fp32  per pair of rows: -lse * log2(e) of both rows, then
+//                                  -rowsum(dO o O) of both; -inf and 0 in the padding
+//                                  (probabilities there are 0)
+//   dQacc [BH][N][d]          fp32  dQ accumulator (unscaled)
 struct WorkspaceLayout {
-    size_t d_off, lse2_off, acc_off, total;
+    size_t stats_off, acc_off, total;
 };
 
 WorkspaceLayout workspace_layout(long long bh, int N, int d_k)
 {
-    const size_t n_pad = ((size_t)N + 63) / 64 * 64;
+    const size_t n_pad = ((size_t)N + 127) / 128 * 128;
     WorkspaceLayout w;
-    w.d_off = 0;
-    w.lse2_off = align256((size_t)bh * n_pad * 4);
-    w.acc_off = w.lse2_off + align256((size_t)bh * n_pad * 4);
+    w.stats_off = 0;
+    w.acc_off = align256((size_t)bh * n_pad * 8);
     w.total = w.acc_off + align256((size_t)bh * N * d_k * 4);
     return w;
 }
@@ -258,12 +258,11 @@ attn_status prepare_bwd(BwdArgs &a, unsigned phases, const void *q, const void *
     a.dq = dq;
     a.dk = dk;
     a.dv = dv;
-    a.dvec = reinterpret_cast<float *>(ws + wl.d_off);
-    a.lse2 = reinterpret_cast<float *>(ws + wl.lse2_off);
+    a.stats = reinterpret_cast<float *>(ws + wl.stats_off);
     a.dq_acc = reinterpret_cast<float *>(ws + wl.acc_off);
     a.bh = (int)bh;
     a.n = N;
-    a.n_pad = (N + 63) / 64 * 64;
+    a.n_pad = (N + 127) / 128 * 128;
     a.d = d_k;
     a.scale = scale;
     a.status = dev->status;

@@ -10,7 +10,7 @@
 //
 // Three stream-ordered kernels:
 //   1. preprocess: -D = -rowsum(dO o O) and -LSE2 = -LSE log2 e (fp32, rows padded to a
-//      multiple of 64 with 0 and -inf so that padded queries get zero probability), and zero
+//      multiple of 128 with 0 and -inf so that padded queries get zero probability), and zero
 //      the fp32 dQ accumulator.
 //   2. main: one CTA per 128-key tile j of one head, looping over all 64-row query tiles i.
 //        warp 12     TMA producer: K_j and V_j once; a ring of (Q_i, dO_i, LSE2_i, D_i).
@@ -59,12 +59,14 @@ struct BwdCfg {
 // ------------------------------------------------------------------ 1. preprocess
 // Over the padded rows (bh, i), i < n_pad, the negated statistics the later kernels add:
 // -D = -sum_c dO_ic O_ic and -LSE2 = -lse log2(e) for i < n; 0 and -inf in the padding (zero
-// probability there).  Then zero the dQ accumulator.
+// probability there), interleaved per pair of rows as {-LSE2_2k, -LSE2_2k+1, -D_2k, -D_2k+1}
+// so that one 16-byte load gives the packed operands for two queries.  Then zero the dQ
+// accumulator.
 template <int D>
 __global__ void __launch_bounds__(256)
     bwd_preprocess_kernel(const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restrict__ dout,
-                          const float *__restrict__ lse, float *__restrict__ dvec,
-                          float *__restrict__ lse2, float *__restrict__ dq_acc, int bh, int n,
+                          const float *__restrict__ lse, float *__restrict__ stats,
+                          float *__restrict__ dq_acc, int bh, int n,
                           int n_pad, int zero_acc)
 {
     constexpr int TPR = D / 8;  // threads per row, 8 bf16 (16 bytes) each
@@ -98,8 +100,9 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
         for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
         if (t < total && part == 0) {
-            dvec[prow] = -acc;
-            lse2[prow] = i < n ? -lse[row] * kLog2e : -INFINITY;
+            float *pair = stats + (prow >> 1) * 4 + (prow & 1);   // n_pad is even
+            pair[0] = i < n ? -lse[row] * kLog2e : -INFINITY;
+            pair[2] = -acc;
         }
     }
     if (!zero_acc) return;
@@ -132,8 +135,7 @@ template <int D, bool WITH_DQ>
 __global__ void __launch_bounds__(448, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                    const float *__restrict__ lse2, const float *__restrict__ dvec,
-                    float *__restrict__ dq_acc, __nv_bfloat16 *__restrict__ dk,
+                    const float *__restrict__ stats, float *__restrict__ dq_acc, __nv_bfloat16 *__restrict__ dk,
                     __nv_bfloat16 *__restrict__ dv, int n, int n_pad, int n_kvblocks, float scale,
                     int *status)
 {
@@ -210,8 +212,7 @@ __global__ void __launch_bounds__(448, 1)
                                      h * 64, it * C::BM, bh);
                 }
                 const size_t rowvec = (size_t)bh * n_pad + (size_t)it * C::BM;
-                ptx::bulk_load(sLD + s * 2 * C::BM, lse2 + rowvec, C::BM * 4, &bar_qf[s]);
-                ptx::bulk_load(sLD + s * 2 * C::BM + C::BM, dvec + rowvec, C::BM * 4, &bar_qf[s]);
+                ptx::bulk_load(sLD + s * 2 * C::BM, stats + rowvec * 2, C::BM * 8, &bar_qf[s]);
             }
             wait_bounded(&bar_kv, 0, g);
             for (int it = (nq > C::QST ? nq - C::QST : 0); it < nq; ++it)
@@ -325,12 +326,13 @@ __global__ void __launch_bounds__(448, 1)
             const int b = wg, s = it % C::QST;
             const uint32_t ph = (it >> 1) & 1;
             // this query tile's -LSE2 (-inf past N) and -D (0 past N), loaded with the tile
-            const float *sl = sLD + s * 2 * C::BM;
-            const float *sd = sl + C::BM;
+            // this tile's {-LSE2 pair, -D pair} per two queries (-inf and 0 past N)
+            const float *sst = sLD + s * 2 * C::BM;
             wait_bounded(&bar_sdp[b], ph, g);
             wait_bounded(&bar_ds_empty[b], ph ^ 1, g);
             ptx::tc_fence_after();
-            uint8_t *rowp = sDS + b * C::DS_BYTES + r * 128;
+            const uint32_t rowp_a = ptx::smem_u32(sDS + b * C::DS_BYTES + r * 128);
+            const uint32_t sst_a = ptx::smem_u32(sst);
             const uint32_t tS = tmem + lane_off + C::tm_s(b), tDP = tmem + lane_off + C::tm_dp(b);
             // 16 queries at a time; the next quarter's TMEM loads overlap this quarter's math.
             // P^T of quarter q goes to columns [8q, 8q + 8), over S^T columns already read.
@@ -349,11 +351,13 @@ __global__ void __launch_bounds__(448, 1)
                 }
                 uint32_t pp[8], dsp[8];
                 const uint64_t c2 = ptx::f2_pack(scale_log2, scale_log2);
+                uint4 st4[8];   // {-LSE2, -LSE2, -D, -D} of queries (c, c + 1), c = 0, 2, ..., 14
+#pragma unroll
+                for (int e = 0; e < 8; ++e) st4[e] = lds_u128(sst_a + (qt * 16 + 2 * e) * 8);
 #pragma unroll
                 for (int c = 0; c < 16; c += 2) {
-                    // nl = -LSE2 and nd = -D of queries c, c + 1 (two fp32 each, packed)
-                    const uint64_t nl = *reinterpret_cast<const uint64_t *>(sl + qt * 16 + c);
-                    const uint64_t nd = *reinterpret_cast<const uint64_t *>(sd + qt * 16 + c);
+                    const uint64_t nl = ((uint64_t)st4[c / 2].y << 32) | st4[c / 2].x;
+                    const uint64_t nd = ((uint64_t)st4[c / 2].w << 32) | st4[c / 2].z;
                     const uint64_t x = ptx::fma_f32x2(
                         ptx::f2_pack(__uint_as_float(sv[cur][c]), __uint_as_float(sv[cur][c + 1])), c2, nl);
                     float x0, x1;
@@ -371,8 +375,8 @@ __global__ void __launch_bounds__(448, 1)
                 ptx::tmem_st8(tS + qt * 8, pp);
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc)
-                    *reinterpret_cast<uint4 *>(rowp + (((qt * 2 + cc) ^ (r & 7)) << 4)) =
-                        make_uint4(dsp[4 * cc], dsp[4 * cc + 1], dsp[4 * cc + 2], dsp[4 * cc + 3]);
+                    sts_u128(rowp_a + (((qt * 2 + cc) ^ (r & 7)) << 4),
+                             make_uint4(dsp[4 * cc], dsp[4 * cc + 1], dsp[4 * cc + 2], dsp[4 * cc + 3]));
                 if (qt < 3) {
                     ptx::tmem_ld_wait();
                     reg_fence(sv[cur ^ 1]);
@@ -434,6 +438,11 @@ __global__ void __launch_bounds__(448, 1)
             // filling one overlaps the bulk reduce-add still reading the other
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
+                // halves past N (only in the last tile) are skipped by every dQ thread alike:
+                // each staged half is one bulk group, which the buffer reuse below counts on
+                const int q0 = it * C::BM + half * 32;
+                if (q0 >= n) break;
+                const int rows = (n - q0) < 32 ? (n - q0) : 32;
                 float *stage = sDQ + half * (C::DQH_BYTES / 4);
                 if (leader) ptx::bulk_wait_group_read<1>();   // this buffer's last reduce has read it
                 ptx::named_bar(2, 128);
@@ -446,12 +455,8 @@ __global__ void __launch_bounds__(448, 1)
                 ptx::fence_proxy_async_smem();
                 ptx::named_bar(2, 128);
                 if (leader) {
-                    const int q0 = it * C::BM + half * 32;
-                    const int rows = (n - q0) < 32 ? (n - q0) : 32;
-                    if (rows > 0) {
-                        ptx::bulk_reduce_add_f32(dq_acc + ((size_t)bh * n + q0) * D, stage, (uint32_t)rows * D * 4);
-                        ptx::bulk_commit_group();
-                    }
+                    ptx::bulk_reduce_add_f32(dq_acc + ((size_t)bh * n + q0) * D, stage, (uint32_t)rows * D * 4);
+                    ptx::bulk_commit_group();
                 }
             }
         }
@@ -461,6 +466,361 @@ __global__ void __launch_bounds__(448, 1)
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == 13) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 512);
+    }
+}
+
+// ------------------------------------------------------------------ 2'. main, d = 64
+// The same products as bwd_main_kernel with 128-query tiles, so that S^T, dP^T and dQ^T run
+// at N = 128 (the full tensor rate; N = 64 runs at two thirds of it) and every per-tile
+// latency is paid once per 128 queries instead of once per 64.
+//   warp 10     TMA: K_j and V_j once; a ring of (Q_i, dO_i, LSE2_i, D_i), 128 rows each.
+//   warp 11     tcgen05, per query tile i (S buffer b = i & 1), once P / dS of tile i are in:
+//                 dP^T and S^T of tile i + 1 first (so that the P / dS warps start on it at
+//                 once), then dV += P^T dO_i, dQ_i^T = K_j^T dS^T (over S^T / P^T of tile i),
+//                 dK += dS^T Q_i.
+//   warps 0-7   both warpgroups on the same tile, warpgroup w on its queries [64w, 64w + 64);
+//               thread = key row.  P^T (bf16) goes over the warpgroup's own S^T columns,
+//               dS^T (bf16) into the warpgroup's 64-query block of the shared dS^T tile.
+//   warps 8-9   dQ_i^T lanes 0-63 (the d rows; lanes 64-127 of the M = 128 product are
+//               unused) from TMEM through shared memory into the fp32 accumulator with bulk
+//               reduce-adds, 32 query rows at a time through two staging buffers.
+// TMEM columns: dK [0,64), dV [64,128), dP^T [128,256), S^T_0 [256,384), S^T_1 [384,512).
+struct WideCfg {
+    static constexpr int D = 64;
+    static constexpr int BN = 128;   // keys per CTA
+    static constexpr int BM = 128;   // queries per tile
+    static constexpr int QST = 3;
+    static constexpr int KV_BYTES = BN * D * 2;
+    static constexpr int Q_BYTES = BM * D * 2;
+    static constexpr int STAGE_BYTES = 2 * Q_BYTES;
+    static constexpr int LD_BYTES = 2 * BM * 4;
+    static constexpr int DS_BYTES = BN * BM * 2;          // two 64-query blocks of BN rows
+    static constexpr int DQC_BYTES = 32 * D * 4;          // dQ staging: 32 query rows
+    static constexpr int SMEM_BYTES =
+        2 * KV_BYTES + QST * STAGE_BYTES + 2 * DS_BYTES + 2 * DQC_BYTES + QST * LD_BYTES + 1024;
+    static constexpr int THREADS = 384;
+    static constexpr int TMA_WARP = 10, MMA_WARP = 11;
+    static constexpr uint32_t TM_DK = 0, TM_DV = 64, TM_DP = 128;
+    __host__ __device__ static constexpr uint32_t tm_s(int b) { return 256 + b * 128; }
+};
+
+__global__ void __launch_bounds__(384, 1)
+    bwd_main_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                         const float *__restrict__ stats, float *__restrict__ dq_acc, __nv_bfloat16 *__restrict__ dk,
+                         __nv_bfloat16 *__restrict__ dv, int n, int n_pad, int n_kvblocks, float scale,
+                         int *status)
+{
+    using C = WideCfg;
+    constexpr int D = C::D;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    uint8_t *sK = smem;
+    uint8_t *sV = sK + C::KV_BYTES;
+    uint8_t *sQ = sV + C::KV_BYTES;                 // QST stages of {Q_i, dO_i}
+    uint8_t *sDS = sQ + C::QST * C::STAGE_BYTES;    // two dS^T tiles
+    float *sDQ = reinterpret_cast<float *>(sDS + 2 * C::DS_BYTES);   // 2 x dQ staging [32][D]
+    float *sLD = reinterpret_cast<float *>(sDS + 2 * C::DS_BYTES + 2 * C::DQC_BYTES);  // QST x {LSE2, D}
+
+    __shared__ uint64_t bar_kv, bar_qf[C::QST], bar_qe[C::QST];
+    __shared__ uint64_t bar_sdp, bar_ds_full, bar_ds_empty[2], bar_dq_full[2], bar_dq_empty[2];
+    __shared__ uint64_t bar_dkv, bar_done;
+    __shared__ uint32_t tmem_sh;
+    __shared__ int abort_sh;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.x / n_kvblocks;
+    const int kv0 = (blockIdx.x % n_kvblocks) * C::BN;
+    const int nq = (n + C::BM - 1) / C::BM;
+    const Guard g{&abort_sh, status, kWaitLimitNs};
+
+    if (threadIdx.x == 0) {
+        abort_sh = 0;
+        ptx::mbar_init(&bar_kv, 1);
+        for (int s = 0; s < C::QST; ++s) {
+            ptx::mbar_init(&bar_qf[s], 1);
+            ptx::mbar_init(&bar_qe[s], 1);
+        }
+        ptx::mbar_init(&bar_sdp, 1);
+        ptx::mbar_init(&bar_ds_full, 256);
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(&bar_ds_empty[b], 1);
+            ptx::mbar_init(&bar_dq_full[b], 1);
+            ptx::mbar_init(&bar_dq_empty[b], 64);
+        }
+        ptx::mbar_init(&bar_dkv, 1);
+        ptx::mbar_init(&bar_done, 1);
+        ptx::fence_mbar_init();
+    }
+    if (warp == C::MMA_WARP) {
+        ptx::tmem_alloc(&tmem_sh, 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = tmem_sh;
+
+    if (warp == C::TMA_WARP) {
+        // ---------------------------------------------------------------- TMA producer
+        if (ptx::elect_one()) {
+            ptx::tma_prefetch_desc(&tm_q);
+            ptx::tma_prefetch_desc(&tm_k);
+            ptx::tma_prefetch_desc(&tm_v);
+            ptx::tma_prefetch_desc(&tm_do);
+            ptx::mbar_arrive_expect_tx(&bar_kv, 2 * C::KV_BYTES);
+            ptx::tma_load_3d(sK, &tm_k, &bar_kv, 0, kv0, bh);
+            ptx::tma_load_3d(sV, &tm_v, &bar_kv, 0, kv0, bh);
+            for (int it = 0; it < nq; ++it) {
+                const int s = it % C::QST;
+                const uint32_t ph = (it / C::QST) & 1;
+                wait_bounded(&bar_qe[s], ph ^ 1, g);
+                ptx::mbar_arrive_expect_tx(&bar_qf[s], C::STAGE_BYTES + C::LD_BYTES);
+                uint8_t *stage = sQ + s * C::STAGE_BYTES;
+                // the Q / dO maps have 64-row boxes: two per 128-row tile, contiguous in the
+                // 128-byte-swizzled layout
+                for (int h = 0; h < 2; ++h) {
+                    ptx::tma_load_3d(stage + h * 64 * 128, &tm_q, &bar_qf[s], 0, it * C::BM + h * 64, bh);
+                    ptx::tma_load_3d(stage + C::Q_BYTES + h * 64 * 128, &tm_do, &bar_qf[s], 0,
+                                     it * C::BM + h * 64, bh);
+                }
+                const size_t rowvec = (size_t)bh * n_pad + (size_t)it * C::BM;
+                ptx::bulk_load(sLD + s * 2 * C::BM, stats + rowvec * 2, C::BM * 8, &bar_qf[s]);
+            }
+            wait_bounded(&bar_kv, 0, g);
+            for (int it = (nq > C::QST ? nq - C::QST : 0); it < nq; ++it)
+                wait_bounded(&bar_qf[it % C::QST], (it / C::QST) & 1, g);
+        }
+    } else if (warp == C::MMA_WARP) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (ptx::elect_one()) {
+            const uint32_t idSdP = ptx::idesc_bf16_f32(128, C::BM, false, false);
+            const uint32_t idKV = ptx::idesc_bf16_f32(128, D, false, true);
+            const uint32_t idDQ = ptx::idesc_bf16_f32(128, C::BM, true, true);
+            const uint32_t k_base = ptx::smem_u32(sK), v_base = ptx::smem_u32(sV);
+            const uint32_t q_base = ptx::smem_u32(sQ), ds_base = ptx::smem_u32(sDS);
+            auto qs = [&](int s) { return q_base + s * C::STAGE_BYTES; };
+            auto dos = [&](int s) { return q_base + s * C::STAGE_BYTES + C::Q_BYTES; };
+            // S^T = K_j Q_i^T and dP^T = V_j dO_i^T: K-major over d, N = 128 query rows.
+            auto issue_s = [&](int s, int b) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    ptx::mma_ss(tmem + C::tm_s(b), ptx::sdesc_sw128(k_base + kk * 32, 16, 1024),
+                                ptx::sdesc_sw128(qs(s) + kk * 32, 16, 1024), idSdP, kk > 0 ? 1u : 0u);
+            };
+            auto issue_dp = [&](int s) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    ptx::mma_ss(tmem + C::TM_DP, ptx::sdesc_sw128(v_base + kk * 32, 16, 1024),
+                                ptx::sdesc_sw128(dos(s) + kk * 32, 16, 1024), idSdP, kk > 0 ? 1u : 0u);
+            };
+            // dV += P^T dO_i: P^T of queries [16kk, 16kk + 16) sits in the S^T columns of the
+            // warpgroup that produced it (64 (kk / 4) + 8 (kk % 4)); dO_i MN-major.
+            auto issue_dv = [&](int s, int b, bool acc) {
+#pragma unroll
+                for (int kk = 0; kk < C::BM / 16; ++kk)
+                    ptx::mma_ts(tmem + C::TM_DV, tmem + C::tm_s(b) + (kk >> 2) * 64 + (kk & 3) * 8,
+                                ptx::sdesc_sw128(dos(s) + kk * 2048, C::BM * 128, 1024), idKV,
+                                (acc || kk > 0) ? 1u : 0u);
+            };
+            // dK += dS^T Q_i: dS^T K-major (two 64-query blocks BN * 128 bytes apart), Q_i MN-major.
+            auto issue_dk = [&](int s, int b, bool acc) {
+#pragma unroll
+                for (int kk = 0; kk < C::BM / 16; ++kk)
+                    ptx::mma_ss(tmem + C::TM_DK,
+                                ptx::sdesc_sw128(ds_base + b * C::DS_BYTES + (kk >> 2) * (C::BN * 128) + (kk & 3) * 32,
+                                                 16, 1024),
+                                ptx::sdesc_sw128(qs(s) + kk * 2048, C::BM * 128, 1024), idKV,
+                                (acc || kk > 0) ? 1u : 0u);
+            };
+            // dQ_i^T = K_j^T dS^T over S^T / P^T of tile i: A = K_j MN-major with M = 128 (rows
+            // 64-127 read V_j, which follows K_j in shared memory, and land in unused lanes),
+            // B = dS^T MN-major, N = 128 queries in two blocks BN * 128 bytes apart.
+            auto issue_dq = [&](int b) {
+#pragma unroll
+                for (int kk = 0; kk < C::BN / 16; ++kk)
+                    ptx::mma_ss(tmem + C::tm_s(b), ptx::sdesc_sw128(k_base + kk * 2048, C::BN * 128, 1024),
+                                ptx::sdesc_sw128(ds_base + b * C::DS_BYTES + kk * 2048, C::BN * 128, 1024),
+                                idDQ, kk > 0 ? 1u : 0u);
+            };
+            wait_bounded(&bar_kv, 0, g);
+            if (nq > 0) {
+                wait_bounded(&bar_qf[0], 0, g);
+                ptx::tc_fence_after();
+                issue_s(0, 0);
+                issue_dp(0);
+                ptx::mma_commit(&bar_sdp);
+            }
+            for (int it = 0; it < nq; ++it) {
+                const int b = it & 1, s = it % C::QST;
+                wait_bounded(&bar_ds_full, it & 1, g);
+                ptx::tc_fence_after();
+                if (it + 1 < nq) {
+                    const int s1 = (it + 1) % C::QST;
+                    wait_bounded(&bar_qf[s1], ((it + 1) / C::QST) & 1, g);
+                    ptx::tc_fence_after();
+                    issue_dp(s1);   // the P / dS warps have read dP^T of tile i
+                    if (it >= 1) wait_bounded(&bar_dq_empty[b ^ 1], ((it - 1) >> 1) & 1, g);
+                    ptx::tc_fence_after();
+                    issue_s(s1, b ^ 1);
+                    ptx::mma_commit(&bar_sdp);
+                }
+                issue_dv(s, b, it > 0);
+                issue_dq(b);
+                ptx::mma_commit(&bar_dq_full[b]);
+                issue_dk(s, b, it > 0);
+                ptx::mma_commit(&bar_qe[s]);
+                ptx::mma_commit(&bar_ds_empty[b]);
+            }
+            ptx::mma_commit(&bar_dkv);
+            ptx::mma_commit(&bar_done);
+            wait_bounded(&bar_done, 0, g);
+        }
+    } else if (warp < 8) {
+        // ---------------------------------------------------------------- P / dS warpgroups
+        const int wg = warp >> 2, cw = warp & 3;
+        const int r = cw * 32 + lane;       // key row within the tile = TMEM lane
+        const bool key_ok = kv0 + r < n;
+        const uint32_t lane_off = (uint32_t)(cw * 32) << 16;
+        const float scale_log2 = scale * kLog2e;
+        for (int it = 0; it < nq; ++it) {
+            const int b = it & 1, s = it % C::QST;
+            // {-LSE2 pair, -D pair} per two of this warpgroup's queries
+            const float *sst = sLD + s * 2 * C::BM + wg * 128;
+            wait_bounded(&bar_sdp, it & 1, g);
+            wait_bounded(&bar_ds_empty[b], ((it >> 1) & 1) ^ 1, g);
+            ptx::tc_fence_after();
+            const uint32_t rowp_a = ptx::smem_u32(sDS + b * C::DS_BYTES + wg * (C::BN * 128) + r * 128);
+            const uint32_t sst_a = ptx::smem_u32(sst);
+            const uint32_t tS = tmem + lane_off + C::tm_s(b) + wg * 64;
+            const uint32_t tDP = tmem + lane_off + C::TM_DP + wg * 64;
+            uint32_t sv[2][16], dpv[2][16];
+            ptx::tmem_ld16(tS, sv[0]);
+            ptx::tmem_ld16(tDP, dpv[0]);
+            ptx::tmem_ld_wait();
+            reg_fence(sv[0]);
+            reg_fence(dpv[0]);
+#pragma unroll
+            for (int qt = 0; qt < 4; ++qt) {
+                const int cur = qt & 1;
+                if (qt < 3) {
+                    ptx::tmem_ld16(tS + (qt + 1) * 16, sv[cur ^ 1]);
+                    ptx::tmem_ld16(tDP + (qt + 1) * 16, dpv[cur ^ 1]);
+                }
+                uint32_t pp[8], dsp[8];
+                const uint64_t c2 = ptx::f2_pack(scale_log2, scale_log2);
+                uint4 st4[8];   // {-LSE2, -LSE2, -D, -D} of queries (c, c + 1), c = 0, 2, ..., 14
+#pragma unroll
+                for (int e = 0; e < 8; ++e) st4[e] = lds_u128(sst_a + (qt * 16 + 2 * e) * 8);
+#pragma unroll
+                for (int c = 0; c < 16; c += 2) {
+                    const uint64_t nl = ((uint64_t)st4[c / 2].y << 32) | st4[c / 2].x;
+                    const uint64_t nd = ((uint64_t)st4[c / 2].w << 32) | st4[c / 2].z;
+                    const uint64_t x = ptx::fma_f32x2(
+                        ptx::f2_pack(__uint_as_float(sv[cur][c]), __uint_as_float(sv[cur][c + 1])), c2, nl);
+                    float x0, x1;
+                    ptx::f2_unpack(x, x0, x1);
+                    float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+                    if (!key_ok) p0 = p1 = 0.f;
+                    const uint64_t pq = ptx::f2_pack(p0, p1);
+                    const uint64_t dsq = ptx::mul_f32x2(
+                        pq, ptx::add_f32x2(ptx::f2_pack(__uint_as_float(dpv[cur][c]), __uint_as_float(dpv[cur][c + 1])), nd));
+                    float ds0, ds1;
+                    ptx::f2_unpack(dsq, ds0, ds1);
+                    pp[c / 2] = ptx::pack_bf16x2(p0, p1);
+                    dsp[c / 2] = ptx::pack_bf16x2(ds0, ds1);
+                }
+                ptx::tmem_st8(tS + qt * 8, pp);
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc)
+                    sts_u128(rowp_a + (((qt * 2 + cc) ^ (r & 7)) << 4),
+                             make_uint4(dsp[4 * cc], dsp[4 * cc + 1], dsp[4 * cc + 2], dsp[4 * cc + 3]));
+                if (qt < 3) {
+                    ptx::tmem_ld_wait();
+                    reg_fence(sv[cur ^ 1]);
+                    reg_fence(dpv[cur ^ 1]);
+                }
+            }
+            ptx::tmem_st_wait();
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&bar_ds_full);
+        }
+        // epilogue: dK = scale * acc, dV = acc, bf16, key rows < n
+        wait_bounded(&bar_dkv, 0, g);
+        ptx::tc_fence_after();
+        const size_t row_off = ((size_t)bh * n + (key_ok ? kv0 + r : 0)) * D;
+        {   // warpgroup 0 writes dK (times scale), warpgroup 1 writes dV
+            const float mul = wg == 0 ? scale : 1.f;
+            __nv_bfloat16 *dst_row = (wg == 0 ? dk : dv) + row_off;
+            const uint32_t col0 = wg == 0 ? C::TM_DK : C::TM_DV;
+#pragma unroll
+            for (int c = 0; c < D; c += 32) {
+                uint32_t v[32];
+                ptx::tmem_ld32(tmem + lane_off + col0 + c, v);
+                ptx::tmem_ld_wait();
+                reg_fence(v);
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    pk[e] = ptx::pack_bf16x2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+                if (key_ok) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(dst_row + c);
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4)
+                        dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                }
+            }
+        }
+    } else if (warp < 10) {
+        // ---------------------------------------------------------------- dQ warps
+        const int r = (warp - 8) * 32 + lane;   // d column = TMEM lane of dQ^T
+        const uint32_t lane_off = (uint32_t)((warp - 8) * 32) << 16;
+        const bool leader = threadIdx.x == 256;
+        int chunk = 0;   // staging buffer = chunk & 1
+        for (int it = 0; it < nq; ++it) {
+            const int b = it & 1;
+            wait_bounded(&bar_dq_full[b], (it >> 1) & 1, g);
+            ptx::tc_fence_after();
+            uint32_t v[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tmem + lane_off + C::tm_s(b) + c * 32, v[c]);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) reg_fence(v[c]);
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&bar_dq_empty[b]);
+            // four chunks of 32 query rows, alternating between two 32 x D staging buffers so
+            // that filling one overlaps the bulk reduce-add still reading the other
+#pragma unroll
+            for (int c = 0; c < 4; ++c, ++chunk) {
+                // Chunks past N (only in the last tile) are skipped by every dQ thread alike:
+                // each staged chunk is one bulk group, which the buffer reuse below counts on.
+                const int q0 = it * C::BM + c * 32;
+                if (q0 >= n) break;
+                const int rows = (n - q0) < 32 ? (n - q0) : 32;
+                float *stage = sDQ + (chunk & 1) * (C::DQC_BYTES / 4);
+                if (leader) ptx::bulk_wait_group_read<1>();   // this buffer's last reduce has read it
+                ptx::named_bar(2, 64);
+                const uint32_t base = opaque(ptx::smem_u32(stage) + r * 4);
+#pragma unroll
+                for (int q = 0; q < 32; ++q) sts_f32(base + q * D * 4, __uint_as_float(v[c][q]));
+                ptx::fence_proxy_async_smem();
+                ptx::named_bar(2, 64);
+                if (leader) {
+                    ptx::bulk_reduce_add_f32(dq_acc + ((size_t)bh * n + q0) * D, stage, (uint32_t)rows * D * 4);
+                    ptx::bulk_commit_group();
+                }
+            }
+        }
+        if (leader) ptx::bulk_wait_group<0>();
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == C::MMA_WARP) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, 512);
     }
@@ -494,8 +854,8 @@ template <int D>
 __global__ void __launch_bounds__(320, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_k64, const __grid_constant__ CUtensorMap tm_v64,
-                  const float *__restrict__ lse2, const float *__restrict__ dvec,
-                  __nv_bfloat16 *__restrict__ dq, int n, int n_pad, int n_qblocks, float scale,
+                  const float *__restrict__ stats, __nv_bfloat16 *__restrict__ dq, int n, int n_pad,
+                  int n_qblocks, float scale,
                   int *status)
 {
     using C = DqCfg<D>;
@@ -636,8 +996,9 @@ __global__ void __launch_bounds__(320, 1)
         const bool row_ok = row < n;
         const uint32_t lane_off = (uint32_t)(cw * 32) << 16;
         const float scale_log2 = scale * kLog2e;
-        const float nl2 = row_ok ? lse2[(size_t)bh * n_pad + row] : -INFINITY;   // -LSE2
-        const float nd = row_ok ? dvec[(size_t)bh * n_pad + row] : 0.f;          // -D
+        const float *pair = stats + ((size_t)bh * n_pad + (row_ok ? row : 0)) / 2 * 4;
+        const float nl2 = row_ok ? pair[row & 1] : -INFINITY;   // -LSE2
+        const float nd = row_ok ? pair[2 + (row & 1)] : 0.f;    // -D
         for (int j = wg; j < nk; j += 2) {
             const int b = wg;
             wait_bounded(&bar_sdp[b], (j >> 1) & 1, g);
@@ -729,7 +1090,7 @@ cudaError_t launch_preprocess_d(const BwdArgs &a, bool zero_acc, cudaStream_t st
 {
     bwd_preprocess_kernel<D><<<elementwise_blocks(), 256, 0, stream>>>(
         reinterpret_cast<const __nv_bfloat16 *>(a.o), reinterpret_cast<const __nv_bfloat16 *>(a.dout),
-        a.lse, a.dvec, a.lse2, a.dq_acc, a.bh, a.n, a.n_pad, zero_acc ? 1 : 0);
+        a.lse, a.stats, a.dq_acc, a.bh, a.n, a.n_pad, zero_acc ? 1 : 0);
     return cudaGetLastError();
 }
 
@@ -743,7 +1104,7 @@ cudaError_t launch_main_d(const BwdArgs &a, cudaStream_t stream)
     const int n_kvblocks = (a.n + C::BN - 1) / C::BN;
     const long long ctas = (long long)n_kvblocks * a.bh;
     bwd_main_kernel<D, WITH_DQ><<<(unsigned)ctas, C::THREADS, C::SMEM_BYTES, stream>>>(
-        a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse2, a.dvec, a.dq_acc,
+        a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.stats, a.dq_acc,
         reinterpret_cast<__nv_bfloat16 *>(a.dk), reinterpret_cast<__nv_bfloat16 *>(a.dv), a.n,
         a.n_pad, n_kvblocks, a.scale, a.status);
     return cudaGetLastError();
@@ -756,9 +1117,24 @@ cudaError_t launch_bwd_preprocess(const BwdArgs &a, cudaStream_t stream)
     return a.d == 64 ? launch_preprocess_d<64>(a, true, stream) : launch_preprocess_d<128>(a, true, stream);
 }
 
+static cudaError_t launch_main_wide(const BwdArgs &a, cudaStream_t stream)
+{
+    using C = WideCfg;
+    cudaError_t e = cudaFuncSetAttribute(bwd_main_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int n_kvblocks = (a.n + C::BN - 1) / C::BN;
+    const long long ctas = (long long)n_kvblocks * a.bh;
+    bwd_main_wide_kernel<<<(unsigned)ctas, C::THREADS, C::SMEM_BYTES, stream>>>(
+        a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.stats, a.dq_acc,
+        reinterpret_cast<__nv_bfloat16 *>(a.dk), reinterpret_cast<__nv_bfloat16 *>(a.dv), a.n,
+        a.n_pad, n_kvblocks, a.scale, a.status);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_bwd_main(const BwdArgs &a, cudaStream_t stream)
 {
-    return a.d == 64 ? launch_main_d<64, true>(a, stream) : launch_main_d<128, true>(a, stream);
+    return a.d == 64 ? launch_main_wide(a, stream) : launch_main_d<128, true>(a, stream);
 }
 
 template <int D>
@@ -771,7 +1147,7 @@ cudaError_t launch_dq_d(const BwdArgs &a, cudaStream_t stream)
     const int n_qblocks = (a.n + C::BM - 1) / C::BM;
     const long long ctas = (long long)n_qblocks * a.bh;
     bwd_dq_kernel<D><<<(unsigned)ctas, C::THREADS, C::SMEM_BYTES, stream>>>(
-        a.tm_q, a.tm_do, a.tm_k64, a.tm_v64, a.lse2, a.dvec,
+        a.tm_q, a.tm_do, a.tm_k64, a.tm_v64, a.stats,
         reinterpret_cast<__nv_bfloat16 *>(a.dq), a.n, a.n_pad, n_qblocks, a.scale, a.status);
     return cudaGetLastError();
 }

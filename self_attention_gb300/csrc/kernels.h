@@ -24,8 +24,9 @@ struct BwdArgs {
     const void *o, *dout;           // [BH, N, d] bf16
     const float *lse;               // [BH, N]
     void *dq, *dk, *dv;             // [BH, N, d] bf16
-    float *dvec;                    // [BH, n_pad] workspace: -rowsum(dO o O), 0 past N
-    float *lse2;                    // [BH, n_pad] workspace: -lse * log2 e, -inf past N
+    // [BH, n_pad / 2] x 4 fp32 workspace, per pair of rows (2k, 2k + 1):
+    // {-lse log2 e of both rows, -rowsum(dO o O) of both rows}; -inf and 0 past N.
+    float *stats;
     float *dq_acc;                  // [BH, N, d]  workspace: fp32 dQ accumulator
     int bh, n, n_pad, d;
     float scale;
