@@ -477,12 +477,14 @@ __global__ void __launch_bounds__(448, 1)
 // latency is paid once per 128 queries instead of once per 64.
 //   warp 10     TMA: K_j and V_j once; a ring of (Q_i, dO_i, LSE2_i, D_i), 128 rows each.
 //   warp 11     tcgen05, per query tile i (S buffer b = i & 1), once P / dS of tile i are in:
-//                 dP^T and S^T of tile i + 1 first (so that the P / dS warps start on it at
-//                 once), then dV += P^T dO_i, dQ_i^T = K_j^T dS^T (over S^T / P^T of tile i),
-//                 dK += dS^T Q_i.
+//                 dP^T of tile i + 1 first, then dV += P^T dO_i, dQ_i^T = K_j^T dS^T (over
+//                 S^T / P^T of tile i), dK += dS^T Q_i, and S^T of tile i + 2 into buffer b as
+//                 soon as dQ_i^T has been drained from it.  S^T of the next tile is thus ready
+//                 when the P / dS warps finish a tile; only dP^T is issued after.
 //   warps 0-7   both warpgroups on the same tile, warpgroup w on its queries [64w, 64w + 64);
-//               thread = key row.  P^T (bf16) goes over the warpgroup's own S^T columns,
-//               dS^T (bf16) into the warpgroup's 64-query block of the shared dS^T tile.
+//               thread = key row.  First P^T from S^T (bf16 over the warpgroup's own S^T
+//               columns, fp32 kept in registers), then, once dP^T is in, dS^T (bf16) into the
+//               warpgroup's 64-query block of the shared dS^T tile.
 //   warps 8-9   dQ_i^T lanes 0-63 (the d rows; lanes 64-127 of the M = 128 product are
 //               unused) from TMEM through shared memory into the fp32 accumulator with bulk
 //               reduce-adds, 32 query rows at a time through two staging buffers.
@@ -525,7 +527,7 @@ __global__ void __launch_bounds__(384, 1)
     float *sLD = reinterpret_cast<float *>(sDS + 2 * C::DS_BYTES + 2 * C::DQC_BYTES);  // QST x {LSE2, D}
 
     __shared__ uint64_t bar_kv, bar_qf[C::QST], bar_qe[C::QST];
-    __shared__ uint64_t bar_sdp, bar_ds_full, bar_ds_empty[2], bar_dq_full[2], bar_dq_empty[2];
+    __shared__ uint64_t bar_s_full[2], bar_dp_full, bar_ds_full, bar_ds_empty[2], bar_dq_full[2], bar_dq_empty[2];
     __shared__ uint64_t bar_dkv, bar_done;
     __shared__ uint32_t tmem_sh;
     __shared__ int abort_sh;
@@ -543,9 +545,10 @@ __global__ void __launch_bounds__(384, 1)
             ptx::mbar_init(&bar_qf[s], 1);
             ptx::mbar_init(&bar_qe[s], 1);
         }
-        ptx::mbar_init(&bar_sdp, 1);
+        ptx::mbar_init(&bar_dp_full, 1);
         ptx::mbar_init(&bar_ds_full, 256);
         for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(&bar_s_full[b], 1);
             ptx::mbar_init(&bar_ds_empty[b], 1);
             ptx::mbar_init(&bar_dq_full[b], 1);
             ptx::mbar_init(&bar_dq_empty[b], 64);
@@ -645,27 +648,29 @@ __global__ void __launch_bounds__(384, 1)
                                 ptx::sdesc_sw128(ds_base + b * C::DS_BYTES + kk * 2048, C::BN * 128, 1024),
                                 idDQ, kk > 0 ? 1u : 0u);
             };
+            // S^T of tile i + 2 goes into buffer b as soon as tile i's dQ^T has been drained from
+            // it, well before the P / dS warps finish tile i + 1; dP^T of tile i + 1 follows
+            // the P / dS warps' last read of dP^T (tile i done).
             wait_bounded(&bar_kv, 0, g);
-            if (nq > 0) {
-                wait_bounded(&bar_qf[0], 0, g);
+            wait_bounded(&bar_qf[0], 0, g);
+            ptx::tc_fence_after();
+            issue_s(0, 0);
+            ptx::mma_commit(&bar_s_full[0]);
+            issue_dp(0);
+            ptx::mma_commit(&bar_dp_full);
+            if (nq > 1) {
+                wait_bounded(&bar_qf[1], 0, g);
                 ptx::tc_fence_after();
-                issue_s(0, 0);
-                issue_dp(0);
-                ptx::mma_commit(&bar_sdp);
+                issue_s(1, 1);
+                ptx::mma_commit(&bar_s_full[1]);
             }
             for (int it = 0; it < nq; ++it) {
                 const int b = it & 1, s = it % C::QST;
                 wait_bounded(&bar_ds_full, it & 1, g);
                 ptx::tc_fence_after();
                 if (it + 1 < nq) {
-                    const int s1 = (it + 1) % C::QST;
-                    wait_bounded(&bar_qf[s1], ((it + 1) / C::QST) & 1, g);
-                    ptx::tc_fence_after();
-                    issue_dp(s1);   // the P / dS warps have read dP^T of tile i
-                    if (it >= 1) wait_bounded(&bar_dq_empty[b ^ 1], ((it - 1) >> 1) & 1, g);
-                    ptx::tc_fence_after();
-                    issue_s(s1, b ^ 1);
-                    ptx::mma_commit(&bar_sdp);
+                    issue_dp((it + 1) % C::QST);   // its Q / dO stage was waited for with its S^T
+                    ptx::mma_commit(&bar_dp_full);
                 }
                 issue_dv(s, b, it > 0);
                 issue_dq(b);
@@ -673,6 +678,14 @@ __global__ void __launch_bounds__(384, 1)
                 issue_dk(s, b, it > 0);
                 ptx::mma_commit(&bar_qe[s]);
                 ptx::mma_commit(&bar_ds_empty[b]);
+                if (it + 2 < nq) {
+                    const int s2 = (it + 2) % C::QST;
+                    wait_bounded(&bar_qf[s2], ((it + 2) / C::QST) & 1, g);
+                    wait_bounded(&bar_dq_empty[b], (it >> 1) & 1, g);   // dQ_i^T drained
+                    ptx::tc_fence_after();
+                    issue_s(s2, b);
+                    ptx::mma_commit(&bar_s_full[b]);
+                }
             }
             ptx::mma_commit(&bar_dkv);
             ptx::mma_commit(&bar_done);
@@ -685,62 +698,88 @@ __global__ void __launch_bounds__(384, 1)
         const bool key_ok = kv0 + r < n;
         const uint32_t lane_off = (uint32_t)(cw * 32) << 16;
         const float scale_log2 = scale * kLog2e;
+        const uint64_t c2 = ptx::f2_pack(scale_log2, scale_log2);
         for (int it = 0; it < nq; ++it) {
             const int b = it & 1, s = it % C::QST;
             // {-LSE2 pair, -D pair} per two of this warpgroup's queries
-            const float *sst = sLD + s * 2 * C::BM + wg * 128;
-            wait_bounded(&bar_sdp, it & 1, g);
-            wait_bounded(&bar_ds_empty[b], ((it >> 1) & 1) ^ 1, g);
-            ptx::tc_fence_after();
+            const uint32_t sst_a = ptx::smem_u32(sLD + s * 2 * C::BM + wg * 128);
             const uint32_t rowp_a = ptx::smem_u32(sDS + b * C::DS_BYTES + wg * (C::BN * 128) + r * 128);
-            const uint32_t sst_a = ptx::smem_u32(sst);
             const uint32_t tS = tmem + lane_off + C::tm_s(b) + wg * 64;
             const uint32_t tDP = tmem + lane_off + C::TM_DP + wg * 64;
-            uint32_t sv[2][16], dpv[2][16];
-            ptx::tmem_ld16(tS, sv[0]);
-            ptx::tmem_ld16(tDP, dpv[0]);
-            ptx::tmem_ld_wait();
-            reg_fence(sv[0]);
-            reg_fence(dpv[0]);
+            wait_bounded(&bar_s_full[b], (it >> 1) & 1, g);
+            wait_bounded(&bar_ds_empty[b], ((it >> 1) & 1) ^ 1, g);
+            ptx::tc_fence_after();
+            // Phase 1, as soon as S^T is in: P^T = 2^(S^T c - LSE2) for 16 queries at a time
+            // (the next 16 columns load meanwhile), bf16 back into TMEM over S^T columns
+            // already read, fp32 kept for dS.
+            float pf[64];
+            {
+                uint32_t sv[2][16];
+                ptx::tmem_ld16(tS, sv[0]);
+                ptx::tmem_ld_wait();
+                reg_fence(sv[0]);
 #pragma unroll
-            for (int qt = 0; qt < 4; ++qt) {
-                const int cur = qt & 1;
-                if (qt < 3) {
-                    ptx::tmem_ld16(tS + (qt + 1) * 16, sv[cur ^ 1]);
-                    ptx::tmem_ld16(tDP + (qt + 1) * 16, dpv[cur ^ 1]);
+                for (int qt = 0; qt < 4; ++qt) {
+                    const int cur = qt & 1;
+                    if (qt < 3) ptx::tmem_ld16(tS + (qt + 1) * 16, sv[cur ^ 1]);
+                    uint2 nl[8];   // -LSE2 of queries (c, c + 1), c = 0, 2, ..., 14
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) nl[e] = lds_u64(sst_a + (qt * 16 + 2 * e) * 8);
+                    uint32_t pp[8];
+#pragma unroll
+                    for (int c = 0; c < 16; c += 2) {
+                        const uint64_t x = ptx::fma_f32x2(
+                            ptx::f2_pack(__uint_as_float(sv[cur][c]), __uint_as_float(sv[cur][c + 1])), c2,
+                            ((uint64_t)nl[c / 2].y << 32) | nl[c / 2].x);
+                        float x0, x1;
+                        ptx::f2_unpack(x, x0, x1);
+                        float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+                        if (!key_ok) p0 = p1 = 0.f;
+                        pf[qt * 16 + c] = p0;
+                        pf[qt * 16 + c + 1] = p1;
+                        pp[c / 2] = ptx::pack_bf16x2(p0, p1);
+                    }
+                    ptx::tmem_st8(tS + qt * 8, pp);
+                    if (qt < 3) {
+                        ptx::tmem_ld_wait();
+                        reg_fence(sv[cur ^ 1]);
+                    }
                 }
-                uint32_t pp[8], dsp[8];
-                const uint64_t c2 = ptx::f2_pack(scale_log2, scale_log2);
-                uint4 st4[8];   // {-LSE2, -LSE2, -D, -D} of queries (c, c + 1), c = 0, 2, ..., 14
+            }
+            // Phase 2, once dP^T is in: dS^T = P^T o (dP^T - D), bf16 into shared memory.
+            wait_bounded(&bar_dp_full, it & 1, g);
+            ptx::tc_fence_after();
+            {
+                uint32_t dpv[2][16];
+                ptx::tmem_ld16(tDP, dpv[0]);
+                ptx::tmem_ld_wait();
+                reg_fence(dpv[0]);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) st4[e] = lds_u128(sst_a + (qt * 16 + 2 * e) * 8);
+                for (int qt = 0; qt < 4; ++qt) {
+                    const int cur = qt & 1;
+                    if (qt < 3) ptx::tmem_ld16(tDP + (qt + 1) * 16, dpv[cur ^ 1]);
+                    uint2 nd[8];   // -D of queries (c, c + 1)
 #pragma unroll
-                for (int c = 0; c < 16; c += 2) {
-                    const uint64_t nl = ((uint64_t)st4[c / 2].y << 32) | st4[c / 2].x;
-                    const uint64_t nd = ((uint64_t)st4[c / 2].w << 32) | st4[c / 2].z;
-                    const uint64_t x = ptx::fma_f32x2(
-                        ptx::f2_pack(__uint_as_float(sv[cur][c]), __uint_as_float(sv[cur][c + 1])), c2, nl);
-                    float x0, x1;
-                    ptx::f2_unpack(x, x0, x1);
-                    float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
-                    if (!key_ok) p0 = p1 = 0.f;
-                    const uint64_t pq = ptx::f2_pack(p0, p1);
-                    const uint64_t dsq = ptx::mul_f32x2(
-                        pq, ptx::add_f32x2(ptx::f2_pack(__uint_as_float(dpv[cur][c]), __uint_as_float(dpv[cur][c + 1])), nd));
-                    float ds0, ds1;
-                    ptx::f2_unpack(dsq, ds0, ds1);
-                    pp[c / 2] = ptx::pack_bf16x2(p0, p1);
-                    dsp[c / 2] = ptx::pack_bf16x2(ds0, ds1);
-                }
-                ptx::tmem_st8(tS + qt * 8, pp);
+                    for (int e = 0; e < 8; ++e) nd[e] = lds_u64(sst_a + (qt * 16 + 2 * e) * 8 + 8);
+                    uint32_t dsp[8];
 #pragma unroll
-                for (int cc = 0; cc < 2; ++cc)
-                    sts_u128(rowp_a + (((qt * 2 + cc) ^ (r & 7)) << 4),
-                             make_uint4(dsp[4 * cc], dsp[4 * cc + 1], dsp[4 * cc + 2], dsp[4 * cc + 3]));
-                if (qt < 3) {
-                    ptx::tmem_ld_wait();
-                    reg_fence(sv[cur ^ 1]);
-                    reg_fence(dpv[cur ^ 1]);
+                    for (int c = 0; c < 16; c += 2) {
+                        const uint64_t dsq = ptx::mul_f32x2(
+                            ptx::f2_pack(pf[qt * 16 + c], pf[qt * 16 + c + 1]),
+                            ptx::add_f32x2(ptx::f2_pack(__uint_as_float(dpv[cur][c]), __uint_as_float(dpv[cur][c + 1])),
+                                           ((uint64_t)nd[c / 2].y << 32) | nd[c / 2].x));
+                        float ds0, ds1;
+                        ptx::f2_unpack(dsq, ds0, ds1);
+                        dsp[c / 2] = ptx::pack_bf16x2(ds0, ds1);
+                    }
+#pragma unroll
+                    for (int cc = 0; cc < 2; ++cc)
+                        sts_u128(rowp_a + (((qt * 2 + cc) ^ (r & 7)) << 4),
+                                 make_uint4(dsp[4 * cc], dsp[4 * cc + 1], dsp[4 * cc + 2], dsp[4 * cc + 3]));
+                    if (qt < 3) {
+                        ptx::tmem_ld_wait();
+                        reg_fence(dpv[cur ^ 1]);
+                    }
                 }
             }
             ptx::tmem_st_wait();

@@ -78,6 +78,13 @@ __device__ __forceinline__ uint4 lds_u128(uint32_t addr)
     return v;
 }
 
+__device__ __forceinline__ uint2 lds_u64(uint32_t addr)
+{
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
+
 __device__ __forceinline__ void sts_u128(uint32_t addr, uint4 v)
 {
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
