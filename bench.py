@@ -472,7 +472,7 @@ def run_ours(args, world, rank, local):
         "fwd_pct_of_bf16_peak": 100.0 * per_gpu_fwd / peaks["bf16_tflops"],
         "bwd_pct_of_bf16_peak": 100.0 * per_gpu_bwd / peaks["bf16_tflops"],
         "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback",
-        "roofline": {"kernel": "bwd_main_kernel<128>" if D == 128 else "bwd_main_kernel<64>",
+        "roofline": {"kernel": "bwd_main_kernel<128>" if D == 128 else "bwd_main_wide_kernel",
                      "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "note": f"peak = {peak_src} sustained dense bf16; achieved = 10*B*H*N^2*d "
