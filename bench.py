@@ -51,7 +51,7 @@ def parse_args(argv=None):
     p.add_argument("--workload", default="long_text")
     p.add_argument("--shape", default=None,
                    help="B,H,N,d override of the workload's sizes (profiling small cases)")
-    p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--oracle-tokens", type=int, default=2048,
                    help="tokens of one head the CPU oracle runs on per reference-arm step")
     p.add_argument("--cpu-baseline-tokens", type=int, default=8192,
@@ -365,32 +365,71 @@ def run_ours(args, world, rank, local):
         "flops": (4.0 + 10.0) * B * H * N * N * D,
     }
 
-    # end to end through the public API: pinned host inputs -> device, forward, backward,
-    # outputs back to pinned host buffers, all inside the timed region
+    # End to end through the C-ABI calls: every step copies its inputs from pinned host memory
+    # to the device, runs attn_fwd and attn_bwd, and copies all outputs (O, LSE, dQ, dK, dV)
+    # back to pinned host memory, all inside the timed region.  The steps are pipelined the way
+    # a training loop feeds a GPU: device buffers are double-buffered and the copies run on
+    # their own streams, so step k+1's inputs arrive and step k-1's outputs leave while step k
+    # computes.
     out_host = {x: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
                 for x, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
-    dev_in = {x: torch.empty_like(host[x], device="cuda") for x in host}
+    dev_in = [{x: torch.empty_like(host[x], device="cuda") for x in host} for _ in range(2)]
+    dev_out = [{x: torch.empty_like(t) for x, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk),
+                                                      ("dv", dv))} for _ in range(2)]
+    s_h2d, s_comp, s_d2h = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()
+    comp_done = [None, None]    # compute of the step that last used buffer j has finished
+    out_copied = [None, None]   # the outputs in buffer j have reached the host
 
-    def e2e_step():
-        for x in host:
-            dev_in[x].copy_(host[x], non_blocking=True)
-        oo, ll = sa.forward(dev_in["q"], dev_in["k"], dev_in["v"], scale)
-        g = sa.backward(dev_in["q"], dev_in["k"], dev_in["v"], oo, dev_in["do"], ll, scale,
-                        workspace=ws)
-        for x, t in zip(("o", "lse", "dq", "dk", "dv"), (oo, ll, *g)):
-            out_host[x].copy_(t, non_blocking=True)
+    def e2e_step(k):
+        j = k & 1
+        di, do_ = dev_in[j], dev_out[j]
+        with torch.cuda.stream(s_h2d):
+            if comp_done[j] is not None:
+                s_h2d.wait_event(comp_done[j])
+            for x in host:
+                di[x].copy_(host[x], non_blocking=True)
+            in_ready = ev()
+            in_ready.record(s_h2d)
+        s_comp.wait_event(in_ready)
+        if out_copied[j] is not None:
+            s_comp.wait_event(out_copied[j])
+        sa.attn_fwd(di["q"], di["k"], di["v"], do_["o"], do_["lse"], B, H, N, D, scale, s_comp)
+        sa.attn_bwd(di["q"], di["k"], di["v"], do_["o"], di["do"], do_["lse"], do_["dq"],
+                    do_["dk"], do_["dv"], ws, ws_bytes, B, H, N, D, scale, s_comp)
+        comp_done[j] = ev()
+        comp_done[j].record(s_comp)
+        with torch.cuda.stream(s_d2h):
+            s_d2h.wait_event(comp_done[j])
+            for x in out_host:
+                out_host[x].copy_(do_[x], non_blocking=True)
+            out_copied[j] = ev()
+            out_copied[j].record(s_d2h)
 
-    e2e_step()
+    def join_all():
+        for st in (s_h2d, s_comp, s_d2h):
+            stream.wait_stream(st)
+
+    for x in (s_h2d, s_comp, s_d2h):
+        x.wait_stream(stream)
+    e2e_step(0)
+    e2e_step(1)
+    join_all()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     e0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
+    for x in (s_h2d, s_comp, s_d2h):
+        x.wait_stream(stream)
+    for k in range(args.e2e_steps):
+        e2e_step(k)
+    join_all()
     e1.record(stream)
     torch.cuda.synchronize()
+    if sa.attn_get_device_status() != 0:
+        raise RuntimeError("device status reported a kernel timeout in the end-to-end loop")
     local_res["e2e_ms"] = e0.elapsed_time(e1) / args.e2e_steps
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in out_host.values())
