@@ -169,8 +169,9 @@ attn_status attn_qkv_proj(const void *x, const void *w_q, const void *w_k, const
 /*
  * Backward of attn_qkv_proj for the gradients dq, dk, dv ([B, H, N, d_k] bf16, e.g. from
  * attn_bwd): dX = sum_t dY_t W_t^T ([B, N, D] bf16 output) and dW_t = X^T dY_t summed over all
- * B*N tokens ([D, D] fp32 outputs, written from zero; the token rows are split across CTAs and
- * their partial sums added with fp32 atomics, so the last bits of dW may vary between runs).
+ * B*N tokens ([D, D] fp32 outputs, written from zero).  Where too few dW tiles exist to fill
+ * the GPU, the token rows are split across CTAs and their partial sums added with fp32 atomics,
+ * so the last bits of dW may then vary between runs.
  * Same size rules as attn_qkv_proj.
  */
 attn_status attn_qkv_proj_bwd(const void *x, const void *w_q, const void *w_k, const void *w_v,
