@@ -155,7 +155,8 @@ extern "C" attn_status attn_fwd(const void *q, const void *k, const void *v, voi
     CUresult r;
     if ((r = make_map(&a.tm_q, q, (int)bh, N, d_k, 128)) != CUDA_SUCCESS ||
         (r = make_map(&a.tm_k, k, (int)bh, N, d_k, 128)) != CUDA_SUCCESS ||
-        (r = make_map(&a.tm_v, v, (int)bh, N, d_k, 128)) != CUDA_SUCCESS)
+        (r = make_map(&a.tm_v, v, (int)bh, N, d_k, 128)) != CUDA_SUCCESS ||
+        (r = make_map(&a.tm_o, o, (int)bh, N, d_k, 128)) != CUDA_SUCCESS)
         return fail_driver("cuTensorMapEncodeTiled", r);
     a.o = o;
     a.lse = lse;

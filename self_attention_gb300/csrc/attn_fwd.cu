@@ -342,7 +342,12 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::THREADS, FwdCfg<D, NQ>::MIN_BLO
 //   warp 5      tcgen05: S = Q K_j^T, O_b += P V_j (b = item parity: two O accumulators, so
 //               an item's products start while the previous item's O is still being written
 //               out); the next S, of this item or the next, follows each P V at once.
-//   warps 0-3   softmax as above, then the epilogue of the item from O_b.
+//   warps 0-3   softmax as above, then the epilogue of the item from O_b: the normalised bf16
+//               tile goes into the item's Q buffer (free once the item's last S has read it),
+//               in the 128-byte-swizzled layout, and leaves with one TMA tensor store (rows
+//               past N are clipped); the Q buffer returns to the producer once the store has
+//               read it.  (One thread per 128-byte row, storing straight to global, makes every
+//               warp store touch 32 lines.)
 // TMEM columns: S [0,128), O_0 [128,128+d), O_1 [128+d,128+2d).
 template <int D>
 struct PersistCfg {
@@ -360,7 +365,7 @@ struct PersistCfg {
 template <int D>
 __global__ void __launch_bounds__(192, 2)
     fwd_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                          const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16 *__restrict__ o,
+                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                           float *__restrict__ lse, int n, int n_qblocks, int n_items,
                           float scale_log2, int *status)
 {
@@ -371,7 +376,7 @@ __global__ void __launch_bounds__(192, 2)
     uint8_t *sK = sQ + 2 * C::Q_BYTES;
     uint8_t *sV = sK + C::STAGES * C::KV_BYTES;
 
-    __shared__ uint64_t bar_qf[2], bar_qe[2];
+    __shared__ uint64_t bar_qf[2], bar_qfree[2];
     __shared__ uint64_t bar_kf[C::STAGES], bar_ke[C::STAGES], bar_vf[C::STAGES], bar_ve[C::STAGES];
     __shared__ uint64_t bar_s, bar_p, bar_of[2], bar_oe[2], bar_done;
     __shared__ uint32_t tmem_sh;
@@ -386,7 +391,7 @@ __global__ void __launch_bounds__(192, 2)
         abort_sh = 0;
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(&bar_qf[b], 1);
-            ptx::mbar_init(&bar_qe[b], 1);
+            ptx::mbar_init(&bar_qfree[b], 1);
             ptx::mbar_init(&bar_of[b], 1);
             ptx::mbar_init(&bar_oe[b], 128);
         }
@@ -421,7 +426,8 @@ __global__ void __launch_bounds__(192, 2)
             for (int item = first; item < n_items; item += stride, ++li) {
                 const int bh = item / n_qblocks, q0 = (item % n_qblocks) * C::BM;
                 const int qb = li & 1;
-                wait_bounded(&bar_qe[qb], ((li >> 1) & 1) ^ 1, g);
+                // Q buffer qb held item li - 2's Q, then its O on the way out
+                wait_bounded(&bar_qfree[qb], ((li >> 1) & 1) ^ 1, g);
                 ptx::mbar_arrive_expect_tx(&bar_qf[qb], C::Q_BYTES);
                 for (int h = 0; h < D / 64; ++h)
                     ptx::tma_load_3d(sQ + qb * C::Q_BYTES + h * C::BM * 128, &tm_q, &bar_qf[qb],
@@ -472,7 +478,7 @@ __global__ void __launch_bounds__(192, 2)
                                 (acc || kk > 0) ? 1u : 0u);
                 }
             };
-            // S of global step kt (item li, key tile j); Q_li is free once its last S is done.
+            // S of global step kt (item li, key tile j)
             auto next_s = [&](int li, int j, int kt) {
                 const int s = kt % C::STAGES;
                 wait_bounded(&bar_kf[s], (kt / C::STAGES) & 1, g);
@@ -481,7 +487,6 @@ __global__ void __launch_bounds__(192, 2)
                 issue_s(li & 1, s);
                 ptx::mma_commit(&bar_s);
                 ptx::mma_commit(&bar_ke[s]);
-                if (j == nkv - 1) ptx::mma_commit(&bar_qe[li & 1]);
             };
             if (first < n_items) next_s(0, 0, 0);
             int kt = 0, li = 0;
@@ -510,11 +515,12 @@ __global__ void __launch_bounds__(192, 2)
         // ---------------------------------------------------------------- softmax warpgroup
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
         const uint32_t tS = tmem + lane_off;
+        const int r_local = warp * 32 + lane;   // row of the tile = TMEM lane
         int kt = 0, li = 0;
         for (int item = first; item < n_items; item += stride, ++li) {
-            const int bh = item / n_qblocks;
-            const int row = (item % n_qblocks) * C::BM + warp * 32 + lane;
-            const int ob = li & 1;
+            const int bh = item / n_qblocks, q0 = (item % n_qblocks) * C::BM;
+            const int row = q0 + r_local;
+            const int ob = li & 1, qb = li & 1;
             const uint32_t tO = tmem + lane_off + C::TM_O + ob * D;
             float m = -INFINITY, l = 0.f;
             for (int j = 0; j < nkv; ++j, ++kt) {
@@ -593,11 +599,13 @@ __global__ void __launch_bounds__(192, 2)
                 ptx::mbar_arrive(&bar_p);
             }
 
-            // epilogue of this item: O = O_b / l (bf16), LSE = (m + log2 l) ln 2
+            // epilogue of this item: O = O_b / l (bf16) into the Q buffer (128-byte swizzle:
+            // 16-byte chunk c of row r at chunk c ^ (r % 8)), then one TMA store of the tile;
+            // LSE = (m + log2 l) ln 2
             wait_bounded(&bar_of[ob], (li >> 1) & 1, g);
             ptx::tc_fence_after();
             const float inv_l = 1.f / l;
-            __nv_bfloat16 *orow = o + ((size_t)bh * n + (row < n ? row : 0)) * D;
+            const uint32_t srow = ptx::smem_u32(sQ + qb * C::Q_BYTES) + r_local * 128;
 #pragma unroll
             for (int c = 0; c < D; c += 32) {
                 uint32_t ov[32];
@@ -609,17 +617,30 @@ __global__ void __launch_bounds__(192, 2)
                 for (int i = 0; i < 16; ++i)
                     pk[i] = ptx::pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l,
                                              __uint_as_float(ov[2 * i + 1]) * inv_l);
-                if (row < n) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c);
+                // columns [c, c + 32) of a 64-column box: chunks (c % 64) / 8 + v4
 #pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4)
-                        dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                for (int v4 = 0; v4 < 4; ++v4) {
+                    const int chunk = ((c & 63) >> 3) + v4;
+                    sts_u128(srow + (c >> 6) * (C::BM * 128) + ((chunk ^ (r_local & 7)) << 4),
+                             make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]));
                 }
             }
             ptx::tc_fence_before();
             ptx::mbar_arrive(&bar_oe[ob]);
+            ptx::fence_proxy_async_smem();
+            ptx::named_bar(1, 128);
+            if (threadIdx.x == 0) {
+                for (int h = 0; h < D / 64; ++h)
+                    ptx::tma_store_3d(&tm_o, sQ + qb * C::Q_BYTES + h * C::BM * 128, h * 64, q0, bh);
+                ptx::bulk_commit_group();
+                // the Q buffer goes back to the producer (for item li + 2) once the store has
+                // read it out of shared memory
+                ptx::bulk_wait_group_read<0>();
+                ptx::mbar_arrive(&bar_qfree[qb]);
+            }
             if (row < n) lse[(size_t)bh * n + row] = (m + log2f(l)) * kLn2;
         }
+        if (threadIdx.x == 0) ptx::bulk_wait_group<0>();   // stores complete before the CTA exits
     }
 
     ptx::tc_fence_before();
@@ -656,7 +677,7 @@ cudaError_t launch_fwd_persistent(const FwdArgs &a, cudaStream_t stream)
     // Two CTAs per SM: TMEM (256 columns each), shared memory and registers are sized for it.
     const long long ctas = std::min<long long>(items, 2LL * sm_count());
     fwd_persistent_kernel<D><<<(unsigned)ctas, C::THREADS, C::SMEM_BYTES, stream>>>(
-        a.tm_q, a.tm_k, a.tm_v, reinterpret_cast<__nv_bfloat16 *>(a.o), a.lse, a.n, n_qblocks,
+        a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.lse, a.n, n_qblocks,
         (int)items, a.scale * kLog2e, a.status);
     return cudaGetLastError();
 }
