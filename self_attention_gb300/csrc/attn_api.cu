@@ -250,7 +250,9 @@ attn_status prepare_bwd(BwdArgs &a, unsigned phases, const void *q, const void *
     if (main && ((r = make_map(&a.tm_q, q, (int)bh, N, d_k, 64)) != CUDA_SUCCESS ||
                  (r = make_map(&a.tm_k, k, (int)bh, N, d_k, 128)) != CUDA_SUCCESS ||
                  (r = make_map(&a.tm_v, v, (int)bh, N, d_k, 128)) != CUDA_SUCCESS ||
-                 (r = make_map(&a.tm_do, dout, (int)bh, N, d_k, 64)) != CUDA_SUCCESS))
+                 (r = make_map(&a.tm_do, dout, (int)bh, N, d_k, 64)) != CUDA_SUCCESS ||
+                 (r = make_map(&a.tm_dk, dk, (int)bh, N, d_k, 128)) != CUDA_SUCCESS ||
+                 (r = make_map(&a.tm_dv, dv, (int)bh, N, d_k, 128)) != CUDA_SUCCESS))
         return fail_driver("cuTensorMapEncodeTiled", r);
     char *ws = static_cast<char *>(workspace);
     a.o = o;

@@ -511,6 +511,7 @@ struct WideCfg {
 __global__ void __launch_bounds__(384, 1)
     bwd_main_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                         const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                          const float *__restrict__ stats, float *__restrict__ dq_acc, __nv_bfloat16 *__restrict__ dk,
                          __nv_bfloat16 *__restrict__ dv, int n, int n_pad, int n_kvblocks, float scale,
                          int *status)
@@ -787,14 +788,15 @@ __global__ void __launch_bounds__(384, 1)
             ptx::tc_fence_before();
             ptx::mbar_arrive(&bar_ds_full);
         }
-        // epilogue: dK = scale * acc, dV = acc, bf16, key rows < n
+        // epilogue: dK = scale * acc (warpgroup 0), dV = acc (warpgroup 1), bf16, staged in the
+        // now idle first (Q, dO) stage in the 128-byte-swizzled layout (16-byte chunk c of row r
+        // at chunk c ^ (r % 8)) and stored with one TMA tensor store each (rows past N clipped)
         wait_bounded(&bar_dkv, 0, g);
         ptx::tc_fence_after();
-        const size_t row_off = ((size_t)bh * n + (key_ok ? kv0 + r : 0)) * D;
-        {   // warpgroup 0 writes dK (times scale), warpgroup 1 writes dV
+        {
             const float mul = wg == 0 ? scale : 1.f;
-            __nv_bfloat16 *dst_row = (wg == 0 ? dk : dv) + row_off;
             const uint32_t col0 = wg == 0 ? C::TM_DK : C::TM_DV;
+            const uint32_t srow = ptx::smem_u32(sQ + wg * C::Q_BYTES) + r * 128;
 #pragma unroll
             for (int c = 0; c < D; c += 32) {
                 uint32_t v[32];
@@ -805,12 +807,18 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
                     pk[e] = ptx::pack_bf16x2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
-                if (key_ok) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(dst_row + c);
 #pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4)
-                        dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
-                }
+                for (int v4 = 0; v4 < 4; ++v4)
+                    sts_u128(srow + ((((c >> 3) + v4) ^ (r & 7)) << 4),
+                             make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]));
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::named_bar(1, 256);
+            if (threadIdx.x == 0) {
+                ptx::tma_store_3d(&tm_dk, sQ, 0, kv0, bh);
+                ptx::tma_store_3d(&tm_dv, sQ + C::Q_BYTES, 0, kv0, bh);
+                ptx::bulk_commit_group();
+                ptx::bulk_wait_group<0>();   // complete before the CTA exits
             }
         }
     } else if (warp < 10) {
@@ -1165,7 +1173,7 @@ static cudaError_t launch_main_wide(const BwdArgs &a, cudaStream_t stream)
     const int n_kvblocks = (a.n + C::BN - 1) / C::BN;
     const long long ctas = (long long)n_kvblocks * a.bh;
     bwd_main_wide_kernel<<<(unsigned)ctas, C::THREADS, C::SMEM_BYTES, stream>>>(
-        a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.stats, a.dq_acc,
+        a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dk, a.tm_dv, a.stats, a.dq_acc,
         reinterpret_cast<__nv_bfloat16 *>(a.dk), reinterpret_cast<__nv_bfloat16 *>(a.dv), a.n,
         a.n_pad, n_kvblocks, a.scale, a.status);
     return cudaGetLastError();
