@@ -473,7 +473,7 @@ __global__ void __launch_bounds__(448, 1)
 
 // ------------------------------------------------------------------ 2'. main, d = 64
 // The same products as bwd_main_kernel with 128-query tiles, so that S^T, dP^T and dQ^T run
-// at N = 128 (the full tensor rate; N = 64 runs at two thirds of it) and every per-tile
+// at N = 128 (an M = 128, K = 16 MMA takes as long at N = 64 as at N = 128) and every per-tile
 // latency is paid once per 128 queries instead of once per 64.
 //   warp 10     TMA: K_j and V_j once; a ring of (Q_i, dO_i, LSE2_i, D_i), 128 rows each.
 //   warp 11     tcgen05, per query tile i (S buffer b = i & 1), once P / dS of tile i are in:
@@ -484,7 +484,9 @@ __global__ void __launch_bounds__(448, 1)
 //   warps 0-7   both warpgroups on the same tile, warpgroup w on its queries [64w, 64w + 64);
 //               thread = key row.  First P^T from S^T (bf16 over the warpgroup's own S^T
 //               columns, fp32 kept in registers), then, once dP^T is in, dS^T (bf16) into the
-//               warpgroup's 64-query block of the shared dS^T tile.
+//               warpgroup's 64-query block of the shared dS^T tile.  At the end dK (warpgroup
+//               0) and dV (warpgroup 1) go through the idle first (Q, dO) stage and leave with
+//               one TMA tensor store each.
 //   warps 8-9   dQ_i^T lanes 0-63 (the d rows; lanes 64-127 of the M = 128 product are
 //               unused) from TMEM through shared memory into the fp32 accumulator with bulk
 //               reduce-adds, 32 query rows at a time through two staging buffers.
@@ -512,9 +514,8 @@ __global__ void __launch_bounds__(384, 1)
     bwd_main_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                          const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
-                         const float *__restrict__ stats, float *__restrict__ dq_acc, __nv_bfloat16 *__restrict__ dk,
-                         __nv_bfloat16 *__restrict__ dv, int n, int n_pad, int n_kvblocks, float scale,
-                         int *status)
+                         const float *__restrict__ stats, float *__restrict__ dq_acc, int n, int n_pad,
+                         int n_kvblocks, float scale, int *status)
 {
     using C = WideCfg;
     constexpr int D = C::D;
@@ -1173,9 +1174,8 @@ static cudaError_t launch_main_wide(const BwdArgs &a, cudaStream_t stream)
     const int n_kvblocks = (a.n + C::BN - 1) / C::BN;
     const long long ctas = (long long)n_kvblocks * a.bh;
     bwd_main_wide_kernel<<<(unsigned)ctas, C::THREADS, C::SMEM_BYTES, stream>>>(
-        a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dk, a.tm_dv, a.stats, a.dq_acc,
-        reinterpret_cast<__nv_bfloat16 *>(a.dk), reinterpret_cast<__nv_bfloat16 *>(a.dv), a.n,
-        a.n_pad, n_kvblocks, a.scale, a.status);
+        a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dk, a.tm_dv, a.stats, a.dq_acc, a.n, a.n_pad, n_kvblocks,
+        a.scale, a.status);
     return cudaGetLastError();
 }
 
