@@ -53,7 +53,7 @@ def run_fwd(inp, scale):
     return o.float().cpu().numpy(), lse.cpu().numpy()
 
 
-EDGE_N = [1, 2, 63, 64, 65, 127, 128, 129, 195, 196, 197, 255, 256, 257, 383, 1000]
+EDGE_N = [1, 2, 63, 64, 65, 127, 128, 129, 195, 196, 197, 255, 256, 257, 383, 1000, 2049, 2500]
 
 
 @pytest.mark.parametrize("d", [64, 128])
