@@ -226,8 +226,10 @@ def time_configs(sa, stream, peaks):
     """Forward and backward (all three phases) of every workload, attention only, on device
     inputs of the workload's shape and distribution.  Warm: back-to-back launches, mean.
     Flushed (the small shapes, whose inputs fit in L2): a 256 MB buffer is written before each
-    launch, outside its events; median.  GB/s counts the algorithmic bytes: forward reads Q, K,
-    V and writes O, LSE; backward reads Q, K, V, O, dO, LSE and writes dQ, dK, dV."""
+    launch, outside its events; median.  Graph (the small shapes): 20 launches captured in a
+    CUDA graph and replayed, mean per launch, without host launch overhead.  GB/s counts the
+    algorithmic bytes: forward reads Q, K, V and writes O, LSE; backward reads Q, K, V, O, dO,
+    LSE and writes dQ, dK, dV."""
     import torch
     from self_attention_gb300.inputs import WORKLOADS
 
@@ -243,9 +245,9 @@ def time_configs(sa, stream, peaks):
         lse = torch.empty(B, H, N, device="cuda")
         wsb = sa.attn_bwd_workspace_size(B, H, N, D)
         ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
-        fwd = lambda: sa.attn_fwd(q, k, v, o, lse, B, H, N, D, w.scale, stream)
-        bwd = lambda: sa.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, wsb, B, H, N, D, w.scale,
-                                  stream)
+        fwd = lambda st=stream: sa.attn_fwd(q, k, v, o, lse, B, H, N, D, w.scale, st)
+        bwd = lambda st=stream: sa.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, wsb, B, H, N, D,
+                                            w.scale, st)
         flops = B * H * N * N * D
         small = 2 * 4 * B * H * N * D < 130e6   # forward inputs + outputs fit in the 129 MB L2
         rep = 200 if small else (20 if flops < 1e11 else 5)
@@ -266,6 +268,27 @@ def time_configs(sa, stream, peaks):
             row[tag + "_tflops"] = fl / us / 1e6
             row[tag + "_gbs"] = nbytes / us / 1e3
             if small:
+                # the same launch captured in a CUDA graph and replayed back to back: the time
+                # without host-side launch overhead (what a captured training step sees)
+                gs = torch.cuda.Stream()
+                gs.wait_stream(stream)
+                with torch.cuda.stream(gs):
+                    fn(gs)
+                gs.synchronize()
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph, stream=gs):
+                    for _ in range(20):
+                        fn(gs)
+                graph.replay()
+                torch.cuda.synchronize()
+                a, b = ev(), ev()
+                a.record(stream)
+                for _ in range(10):
+                    graph.replay()
+                b.record(stream)
+                torch.cuda.synchronize()
+                row[tag + "_us_graph"] = a.elapsed_time(b) / 200 * 1e3
+                del graph
                 ts = []
                 for _ in range(30):
                     flush.fill_(1)

@@ -1,0 +1,69 @@
+"""The C-ABI calls enqueue only on the stream they are given and never synchronise, so a whole
+forward + backward step can be captured once in a CUDA graph and replayed: replays with new
+inputs copied into the captured buffers must give what eager calls give."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import self_attention_gb300 as sa
+from self_attention_gb300.inputs import make_qkv
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from self_attention_gb300.build import build
+    sa.load_library(build())
+
+
+@pytest.mark.parametrize("shape", [(4, 12, 196, 64), (1, 4, 1000, 128)])
+def test_graph_replay_matches_eager(shape):
+    B, H, N, D = shape
+    scale = 1.0 / math.sqrt(D)
+    dev = lambda t: t.cuda()
+    bufs = {x: torch.empty(B, H, N, D, dtype=torch.bfloat16, device="cuda") for x in ("q", "k", "v", "do")}
+    o, dq, dk, dv = (torch.empty(B, H, N, D, dtype=torch.bfloat16, device="cuda") for _ in range(4))
+    lse = torch.empty(B, H, N, device="cuda")
+    wsb = sa.attn_bwd_workspace_size(B, H, N, D)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+
+    def step():
+        sa.attn_fwd(bufs["q"], bufs["k"], bufs["v"], o, lse, B, H, N, D, scale, s)
+        sa.attn_bwd(bufs["q"], bufs["k"], bufs["v"], o, bufs["do"], lse, dq, dk, dv, ws, wsb, B, H, N,
+                    D, scale, s)
+
+    first = make_qkv(B, H, N, D, seed=9100 + N, with_do=True)
+    for x in bufs:
+        bufs[x].copy_(first[x])
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):   # warm-up outside the capture (loads the kernels)
+        step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step()
+    torch.cuda.synchronize()
+
+    for seed in (9200 + N, 9300 + N):
+        inp = make_qkv(B, H, N, D, seed=seed, with_do=True)
+        for x in bufs:
+            bufs[x].copy_(inp[x])
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert sa.attn_get_device_status() == 0
+        replay = {n_: t.float().cpu().numpy() for n_, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+        ref_o, ref_lse = sa.forward(*(dev(inp[x]) for x in ("q", "k", "v")), scale)
+        ref_dq, ref_dk, ref_dv = sa.backward(*(dev(inp[x]) for x in ("q", "k", "v")), ref_o, dev(inp["do"]),
+                                             ref_lse, scale)
+        eager = {n_: t.float().cpu().numpy() for n_, t in (("o", ref_o), ("lse", ref_lse), ("dq", ref_dq), ("dk", ref_dk), ("dv", ref_dv))}
+        # forward, dK and dV involve no atomics: bitwise equal; dQ sums fp32 partials in any order
+        for n_ in ("o", "lse", "dk", "dv"):
+            np.testing.assert_array_equal(replay[n_], eager[n_], err_msg=n_)
+        np.testing.assert_allclose(replay["dq"], eager["dq"], rtol=2 ** -7, atol=2 ** -12)
