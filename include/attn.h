@@ -24,6 +24,8 @@
  *     workspace.  The library allocates no device memory on these paths.
  *   - Calls enqueue work on `stream` and return without waiting; only
  *     attn_get_device_status() synchronises (that stream).  Outputs must not overlap inputs.
+ *   - The compute calls allocate nothing and never synchronise, so they may be captured in a
+ *     CUDA graph on `stream` and replayed (the captured pointers, sizes and scale are fixed).
  *   - Errors: every argument check runs before any launch; on failure the call returns a
  *     non-zero attn_status and launches nothing.  A kernel that cannot make progress does not
  *     hang the GPU: each of its waits gives up after a bounded time and records
