@@ -335,11 +335,6 @@ extern "C" attn_status attn_bwd_deterministic(const void *q, const void *k, cons
     attn_status st = prepare_bwd(a, kPre | kMain | kConv, q, k, v, o, dout, lse, dq, dk, dv,
                                  workspace, workspace_bytes, B, H, N, d_k, scale);
     if (st != ATTN_OK) return st;
-    CUresult r;
-    const int bh = B * H;
-    if ((r = make_map(&a.tm_k64, k, bh, N, d_k, 64)) != CUDA_SUCCESS ||
-        (r = make_map(&a.tm_v64, v, bh, N, d_k, 64)) != CUDA_SUCCESS)
-        return fail_driver("cuTensorMapEncodeTiled", r);
     const cudaError_t e = launch_bwd_deterministic(a, stream);
     return e == cudaSuccess ? ATTN_OK : fail("attn_bwd_deterministic launch", e);
 }

@@ -876,45 +876,50 @@ __global__ void __launch_bounds__(384, 1)
 
 // ------------------------------------------------------------------ 4. deterministic dQ pass
 // dQ_i = scale * sum_j dS_ij K_j without atomics: one CTA owns 128 query rows of one head and
-// walks the key tiles (64 keys each) in order, recomputing S = Q K^T and dP = dO V^T on chip.
-//   warp 8      TMA: Q_i and dO_i once; a ring of (K_j, V_j).
-//   warp 9      tcgen05: S_j, dP_j into TMEM (two buffers), then dQ += dS_j K_j with dS_j read
-//               from TMEM (bf16, written over S_j) and K_j MN-major from shared memory.
-//   warps 0-7   two warpgroups, alternating key tiles; thread = query row, whose LSE and D
-//               sit in registers: P = 2^(S c - LSE log2 e), dS = P o (dP - D).
-// TMEM: S_0 [0,64), dP_0 [64,128), S_1 [128,192), dP_1 [192,256), dQ [256,256+d).
+// walks the key tiles (128 keys each) in order, recomputing S = Q K^T and dP = dO V^T on chip.
+// With 128-key steps S and dP run at N = 128 (an M = 128 MMA takes as long at N = 64).
+//   warp 8      TMA: Q_i and dO_i once; a ring of K_j and a ring of V_j.
+//   warp 9      tcgen05, per key tile j (S buffer b = j & 1), once dS_j is in: dP of tile
+//               j + 1 first (the P / dS warps have read dP_j), then dQ += dS_j K_j (dS_j read
+//               from TMEM, bf16 over S_j; K_j MN-major), then S of tile j + 2 into buffer b
+//               (issued after the dQ product that reads it, so in order).
+//   warps 0-7   both warpgroups on the same key tile, warpgroup h on its keys [64h, 64h + 64);
+//               thread = query row, whose LSE and D sit in registers.  First P = 2^(S c - LSE
+//               log2 e) as soon as S_j is in (fp32 kept), then dS = P o (dP - D) once dP_j is
+//               in, bf16 over the warpgroup's own S columns (keys [64h, 64h + 64) -> columns
+//               [64h, 64h + 32)).
+// TMEM: S_0 [0,128), S_1 [128,256), dP [256,384), dQ [384,384+d).
 template <int D>
 struct DqCfg {
     static constexpr int BM = 128;   // query rows per CTA
-    static constexpr int BN = 64;    // keys per step
-    static constexpr int STAGES = (D == 64) ? 6 : 4;
+    static constexpr int BN = 128;   // keys per step
+    static constexpr int KST = (D == 64) ? 4 : 3;   // K ring
+    static constexpr int VST = (D == 64) ? 3 : 2;   // V ring (V is read only by dP, one step ahead)
     static constexpr int Q_BYTES = BM * D * 2;
     static constexpr int KV_BYTES = BN * D * 2;
-    static constexpr int STAGE_BYTES = 2 * KV_BYTES;   // K_j then V_j
-    static constexpr int SMEM_BYTES = 2 * Q_BYTES + STAGES * STAGE_BYTES + 1024;
+    static constexpr int SMEM_BYTES = 2 * Q_BYTES + (KST + VST) * KV_BYTES + 1024;
     static constexpr int THREADS = 320;
-    static constexpr uint32_t TM_DQ = 256;
+    static constexpr uint32_t TM_DP = 256, TM_DQ = 384;
     __host__ __device__ static constexpr uint32_t tm_s(int b) { return b * 128; }
-    __host__ __device__ static constexpr uint32_t tm_dp(int b) { return b * 128 + 64; }
 };
 
 template <int D>
 __global__ void __launch_bounds__(320, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
-                  const __grid_constant__ CUtensorMap tm_k64, const __grid_constant__ CUtensorMap tm_v64,
+                  const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const float *__restrict__ stats, __nv_bfloat16 *__restrict__ dq, int n, int n_pad,
-                  int n_qblocks, float scale,
-                  int *status)
+                  int n_qblocks, float scale, int *status)
 {
     using C = DqCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
-    uint8_t *sQ = smem;                      // Q_i: two 64-column halves of 128 rows
+    uint8_t *sQ = smem;                      // Q_i: d / 64 column blocks of 128 rows
     uint8_t *sdO = sQ + C::Q_BYTES;          // dO_i, same layout
-    uint8_t *sKV = sdO + C::Q_BYTES;         // STAGES x {K_j, V_j}
+    uint8_t *sK = sdO + C::Q_BYTES;          // KST x K_j
+    uint8_t *sV = sK + C::KST * C::KV_BYTES; // VST x V_j
 
-    __shared__ uint64_t bar_q, bar_kvf[C::STAGES], bar_kve[C::STAGES];
-    __shared__ uint64_t bar_sdp[2], bar_ds[2], bar_dq, bar_done;
+    __shared__ uint64_t bar_q, bar_kf[C::KST], bar_ke[C::KST], bar_vf[C::VST], bar_ve[C::VST];
+    __shared__ uint64_t bar_s_full[2], bar_dp_full, bar_ds_full, bar_dq, bar_done;
     __shared__ uint32_t tmem_sh;
     __shared__ int abort_sh;
 
@@ -927,14 +932,17 @@ __global__ void __launch_bounds__(320, 1)
     if (threadIdx.x == 0) {
         abort_sh = 0;
         ptx::mbar_init(&bar_q, 1);
-        for (int s = 0; s < C::STAGES; ++s) {
-            ptx::mbar_init(&bar_kvf[s], 1);
-            ptx::mbar_init(&bar_kve[s], 1);
+        for (int s = 0; s < C::KST; ++s) {
+            ptx::mbar_init(&bar_kf[s], 1);
+            ptx::mbar_init(&bar_ke[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            ptx::mbar_init(&bar_sdp[b], 1);
-            ptx::mbar_init(&bar_ds[b], 128);
+        for (int s = 0; s < C::VST; ++s) {
+            ptx::mbar_init(&bar_vf[s], 1);
+            ptx::mbar_init(&bar_ve[s], 1);
         }
+        for (int b = 0; b < 2; ++b) ptx::mbar_init(&bar_s_full[b], 1);
+        ptx::mbar_init(&bar_dp_full, 1);
+        ptx::mbar_init(&bar_ds_full, 256);
         ptx::mbar_init(&bar_dq, 1);
         ptx::mbar_init(&bar_done, 1);
         ptx::fence_mbar_init();
@@ -953,29 +961,34 @@ __global__ void __launch_bounds__(320, 1)
         if (ptx::elect_one()) {
             ptx::tma_prefetch_desc(&tm_q);
             ptx::tma_prefetch_desc(&tm_do);
-            ptx::tma_prefetch_desc(&tm_k64);
-            ptx::tma_prefetch_desc(&tm_v64);
+            ptx::tma_prefetch_desc(&tm_k);
+            ptx::tma_prefetch_desc(&tm_v);
+            // the Q / dO maps have 64-row boxes: two per 128-row tile, contiguous in the
+            // 128-byte-swizzled layout; d = 128 tiles are two 64-column blocks of 16 KB
             ptx::mbar_arrive_expect_tx(&bar_q, 2 * C::Q_BYTES);
             for (int h = 0; h < D / 64; ++h)
-                for (int rb = 0; rb < 2; ++rb) {
-                    ptx::tma_load_3d(sQ + h * C::BM * 128 + rb * 8192, &tm_q, &bar_q, h * 64, q0 + rb * 64, bh);
-                    ptx::tma_load_3d(sdO + h * C::BM * 128 + rb * 8192, &tm_do, &bar_q, h * 64, q0 + rb * 64, bh);
+                for (int r = 0; r < 2; ++r) {
+                    ptx::tma_load_3d(sQ + h * C::BM * 128 + r * 64 * 128, &tm_q, &bar_q, h * 64, q0 + r * 64, bh);
+                    ptx::tma_load_3d(sdO + h * C::BM * 128 + r * 64 * 128, &tm_do, &bar_q, h * 64, q0 + r * 64, bh);
                 }
+            // K_j and V_j in key order; V runs at most VST tiles ahead of dP, K at most KST
+            // tiles ahead of dQ
             for (int j = 0; j < nk; ++j) {
-                const int s = j % C::STAGES;
-                const uint32_t ph = (j / C::STAGES) & 1;
-                wait_bounded(&bar_kve[s], ph ^ 1, g);
-                ptx::mbar_arrive_expect_tx(&bar_kvf[s], C::STAGE_BYTES);
-                uint8_t *stage = sKV + s * C::STAGE_BYTES;
-                for (int h = 0; h < D / 64; ++h) {
-                    ptx::tma_load_3d(stage + h * C::BN * 128, &tm_k64, &bar_kvf[s], h * 64, j * C::BN, bh);
-                    ptx::tma_load_3d(stage + C::KV_BYTES + h * C::BN * 128, &tm_v64, &bar_kvf[s],
-                                     h * 64, j * C::BN, bh);
-                }
+                const int sk = j % C::KST, sv = j % C::VST;
+                wait_bounded(&bar_ke[sk], ((j / C::KST) & 1) ^ 1, g);
+                ptx::mbar_arrive_expect_tx(&bar_kf[sk], C::KV_BYTES);
+                for (int h = 0; h < D / 64; ++h)
+                    ptx::tma_load_3d(sK + sk * C::KV_BYTES + h * C::BN * 128, &tm_k, &bar_kf[sk], h * 64, j * C::BN, bh);
+                wait_bounded(&bar_ve[sv], ((j / C::VST) & 1) ^ 1, g);
+                ptx::mbar_arrive_expect_tx(&bar_vf[sv], C::KV_BYTES);
+                for (int h = 0; h < D / 64; ++h)
+                    ptx::tma_load_3d(sV + sv * C::KV_BYTES + h * C::BN * 128, &tm_v, &bar_vf[sv], h * 64, j * C::BN, bh);
             }
             wait_bounded(&bar_q, 0, g);
-            for (int j = (nk > C::STAGES ? nk - C::STAGES : 0); j < nk; ++j)
-                wait_bounded(&bar_kvf[j % C::STAGES], (j / C::STAGES) & 1, g);
+            for (int j = (nk > C::VST ? nk - C::VST : 0); j < nk; ++j)
+                wait_bounded(&bar_vf[j % C::VST], (j / C::VST) & 1, g);
+            for (int j = (nk > C::KST ? nk - C::KST : 0); j < nk; ++j)
+                wait_bounded(&bar_kf[j % C::KST], (j / C::KST) & 1, g);
         }
     } else if (warp == 9) {
         // ---------------------------------------------------------------- MMA issuer
@@ -983,55 +996,66 @@ __global__ void __launch_bounds__(320, 1)
             const uint32_t idSP = ptx::idesc_bf16_f32(128, C::BN, false, false);
             const uint32_t idQ = ptx::idesc_bf16_f32(128, D, false, true);
             const uint32_t q_base = ptx::smem_u32(sQ), do_base = ptx::smem_u32(sdO),
-                           kv_base = ptx::smem_u32(sKV);
-            auto kst = [&](int s) { return kv_base + s * C::STAGE_BYTES; };
-            // S_j = Q K_j^T and dP_j = dO V_j^T: all operands K-major over d.
-            auto issue_sdp = [&](int s, int b) {
+                           k_base = ptx::smem_u32(sK), v_base = ptx::smem_u32(sV);
+            // S_j = Q K_j^T and dP_j = dO V_j^T: all operands K-major over d (64-column blocks
+            // BM * 128 / BN * 128 bytes apart), N = 128 keys.
+            auto issue_s = [&](int sk, int b) {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t offa = (kk >> 2) * (C::BM * 128) + (kk & 3) * 32;
                     const uint32_t offb = (kk >> 2) * (C::BN * 128) + (kk & 3) * 32;
                     ptx::mma_ss(tmem + C::tm_s(b), ptx::sdesc_sw128(q_base + offa, 16, 1024),
-                                ptx::sdesc_sw128(kst(s) + offb, 16, 1024), idSP, kk > 0 ? 1u : 0u);
+                                ptx::sdesc_sw128(k_base + sk * C::KV_BYTES + offb, 16, 1024), idSP,
+                                kk > 0 ? 1u : 0u);
                 }
+            };
+            auto issue_dp = [&](int sv) {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t offa = (kk >> 2) * (C::BM * 128) + (kk & 3) * 32;
                     const uint32_t offb = (kk >> 2) * (C::BN * 128) + (kk & 3) * 32;
-                    ptx::mma_ss(tmem + C::tm_dp(b), ptx::sdesc_sw128(do_base + offa, 16, 1024),
-                                ptx::sdesc_sw128(kst(s) + C::KV_BYTES + offb, 16, 1024), idSP,
+                    ptx::mma_ss(tmem + C::TM_DP, ptx::sdesc_sw128(do_base + offa, 16, 1024),
+                                ptx::sdesc_sw128(v_base + sv * C::KV_BYTES + offb, 16, 1024), idSP,
                                 kk > 0 ? 1u : 0u);
                 }
             };
-            // dQ += dS_j K_j: A = dS_j (TMEM, 8 columns per 16 keys), B = K_j MN-major
-            // (K = keys, N = d; 64-column halves BN*128 bytes apart).
-            auto issue_dq = [&](int s, int b, bool acc) {
+            // dQ += dS_j K_j: A = dS_j from TMEM (keys [16kk, 16kk + 16) in the columns of the
+            // warpgroup that wrote them: 64 (kk / 4) + 8 (kk % 4)), B = K_j MN-major (K = keys,
+            // N = d; 64-column blocks BN * 128 bytes apart).
+            auto issue_dq = [&](int sk, int b, bool acc) {
 #pragma unroll
                 for (int kk = 0; kk < C::BN / 16; ++kk)
-                    ptx::mma_ts(tmem + C::TM_DQ, tmem + C::tm_s(b) + kk * 8,
-                                ptx::sdesc_sw128(kst(s) + kk * 2048, C::BN * 128, 1024), idQ,
+                    ptx::mma_ts(tmem + C::TM_DQ, tmem + C::tm_s(b) + (kk >> 2) * 64 + (kk & 3) * 8,
+                                ptx::sdesc_sw128(k_base + sk * C::KV_BYTES + kk * 2048, C::BN * 128, 1024), idQ,
                                 (acc || kk > 0) ? 1u : 0u);
             };
+            auto start_s = [&](int j) {
+                wait_bounded(&bar_kf[j % C::KST], (j / C::KST) & 1, g);
+                ptx::tc_fence_after();
+                issue_s(j % C::KST, j & 1);
+                ptx::mma_commit(&bar_s_full[j & 1]);
+            };
+            auto start_dp = [&](int j) {
+                wait_bounded(&bar_vf[j % C::VST], (j / C::VST) & 1, g);
+                ptx::tc_fence_after();
+                issue_dp(j % C::VST);
+                ptx::mma_commit(&bar_dp_full);
+                ptx::mma_commit(&bar_ve[j % C::VST]);
+            };
             wait_bounded(&bar_q, 0, g);
-            for (int j = 0; j < 2 && j < nk; ++j) {
-                wait_bounded(&bar_kvf[j % C::STAGES], (j / C::STAGES) & 1, g);
-                ptx::tc_fence_after();
-                issue_sdp(j % C::STAGES, j);
-                ptx::mma_commit(&bar_sdp[j]);
+            if (nk > 0) {
+                start_s(0);
+                start_dp(0);
             }
+            if (nk > 1) start_s(1);
             for (int j = 0; j < nk; ++j) {
-                const int b = j & 1, s = j % C::STAGES;
-                wait_bounded(&bar_ds[b], (j >> 1) & 1, g);
+                const int b = j & 1, sk = j % C::KST;
+                wait_bounded(&bar_ds_full, j & 1, g);
                 ptx::tc_fence_after();
-                issue_dq(s, b, j > 0);
-                ptx::mma_commit(&bar_kve[s]);
-                if (j + 2 < nk) {
-                    const int s2 = (j + 2) % C::STAGES;
-                    wait_bounded(&bar_kvf[s2], ((j + 2) / C::STAGES) & 1, g);
-                    ptx::tc_fence_after();
-                    issue_sdp(s2, b);
-                    ptx::mma_commit(&bar_sdp[b]);
-                }
+                if (j + 1 < nk) start_dp(j + 1);   // the P / dS warps have read dP_j
+                issue_dq(sk, b, j > 0);
+                ptx::mma_commit(&bar_ke[sk]);      // K_j: S_j and dQ_j done with it
+                if (j + 2 < nk) start_s(j + 2);    // over dS_j, after the dQ product that reads it
             }
             ptx::mma_commit(&bar_dq);
             ptx::mma_commit(&bar_done);
@@ -1039,7 +1063,7 @@ __global__ void __launch_bounds__(320, 1)
         }
     } else {
         // ---------------------------------------------------------------- P / dS warpgroups
-        const int wg = warp >> 2, cw = warp & 3;
+        const int h = warp >> 2, cw = warp & 3;
         const int row = q0 + cw * 32 + lane;    // query row = TMEM lane
         const bool row_ok = row < n;
         const uint32_t lane_off = (uint32_t)(cw * 32) << 16;
@@ -1047,54 +1071,64 @@ __global__ void __launch_bounds__(320, 1)
         const float *pair = stats + ((size_t)bh * n_pad + (row_ok ? row : 0)) / 2 * 4;
         const float nl2 = row_ok ? pair[row & 1] : -INFINITY;   // -LSE2
         const float nd = row_ok ? pair[2 + (row & 1)] : 0.f;    // -D
-        for (int j = wg; j < nk; j += 2) {
-            const int b = wg;
-            wait_bounded(&bar_sdp[b], (j >> 1) & 1, g);
+        const uint64_t c2 = ptx::f2_pack(scale_log2, scale_log2), nl22 = ptx::f2_pack(nl2, nl2),
+                       nd2 = ptx::f2_pack(nd, nd);
+        for (int j = 0; j < nk; ++j) {
+            const int b = j & 1;
+            const int valid = n - j * C::BN - h * 64;   // keys of this warpgroup below n
+            const uint32_t tS = tmem + lane_off + C::tm_s(b) + h * 64, tDP = tmem + lane_off + C::TM_DP + h * 64;
+            wait_bounded(&bar_s_full[b], (j >> 1) & 1, g);
             ptx::tc_fence_after();
-            const int valid = n - j * C::BN;   // keys of this tile below n
-            const uint32_t tS = tmem + lane_off + C::tm_s(b), tDP = tmem + lane_off + C::tm_dp(b);
-            // 16 keys at a time; dS of quarter q goes to columns [8q, 8q + 8), over S already read
-            uint32_t sv[2][16], dpv[2][16];
-            ptx::tmem_ld16(tS, sv[0]);
-            ptx::tmem_ld16(tDP, dpv[0]);
-            ptx::tmem_ld_wait();
-            reg_fence(sv[0]);
-            reg_fence(dpv[0]);
+            // phase 1, as soon as S_j is in: P for this warpgroup's 64 keys (fp32 kept)
+            float pf[64];
 #pragma unroll
-            for (int qt = 0; qt < 4; ++qt) {
-                const int cur = qt & 1;
-                if (qt < 3) {
-                    ptx::tmem_ld16(tS + (qt + 1) * 16, sv[cur ^ 1]);
-                    ptx::tmem_ld16(tDP + (qt + 1) * 16, dpv[cur ^ 1]);
-                }
-                uint32_t dsp[8];
+            for (int c = 0; c < 64; c += 32) {
+                uint32_t sv[32];
+                ptx::tmem_ld32(tS + c, sv);
+                ptx::tmem_ld_wait();
+                reg_fence(sv);
 #pragma unroll
-                for (int c = 0; c < 16; c += 2) {
-                    float p0 = ptx::ex2(fmaf(__uint_as_float(sv[cur][c]), scale_log2, nl2));
-                    float p1 = ptx::ex2(fmaf(__uint_as_float(sv[cur][c + 1]), scale_log2, nl2));
-                    if (qt * 16 + c >= valid) p0 = 0.f;
-                    if (qt * 16 + c + 1 >= valid) p1 = 0.f;
-                    dsp[c / 2] = ptx::pack_bf16x2(p0 * (__uint_as_float(dpv[cur][c]) + nd),
-                                                  p1 * (__uint_as_float(dpv[cur][c + 1]) + nd));
+                for (int i = 0; i < 32; i += 2) {
+                    const uint64_t x = ptx::fma_f32x2(ptx::f2_pack(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), c2, nl22);
+                    float x0, x1;
+                    ptx::f2_unpack(x, x0, x1);
+                    pf[c + i] = c + i < valid ? ptx::ex2(x0) : 0.f;
+                    pf[c + i + 1] = c + i + 1 < valid ? ptx::ex2(x1) : 0.f;
                 }
-                ptx::tmem_st8(tS + qt * 8, dsp);
-                if (qt < 3) {
-                    ptx::tmem_ld_wait();
-                    reg_fence(sv[cur ^ 1]);
-                    reg_fence(dpv[cur ^ 1]);
+            }
+            // phase 2, once dP_j is in: dS = P o (dP - D), bf16 over this warpgroup's S columns
+            // (read in phase 1): keys [64h + c, +32) -> columns 64h + c / 2 + [0, 16)
+            wait_bounded(&bar_dp_full, j & 1, g);
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < 64; c += 32) {
+                uint32_t dpv[32];
+                ptx::tmem_ld32(tDP + c, dpv);
+                ptx::tmem_ld_wait();
+                reg_fence(dpv);
+                uint32_t dsp[16];
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    const uint64_t dsq = ptx::mul_f32x2(
+                        ptx::f2_pack(pf[c + i], pf[c + i + 1]),
+                        ptx::add_f32x2(ptx::f2_pack(__uint_as_float(dpv[i]), __uint_as_float(dpv[i + 1])), nd2));
+                    float ds0, ds1;
+                    ptx::f2_unpack(dsq, ds0, ds1);
+                    dsp[i / 2] = ptx::pack_bf16x2(ds0, ds1);
                 }
+                ptx::tmem_st16(tS + c / 2, dsp);
             }
             ptx::tmem_st_wait();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(&bar_ds[b]);
+            ptx::mbar_arrive(&bar_ds_full);
         }
-        // epilogue: dQ = scale * acc in bf16; warpgroup wg writes columns [wg*D/2, (wg+1)*D/2)
+        // epilogue: dQ = scale * acc in bf16; warpgroup h writes columns [h*D/2, (h+1)*D/2)
         wait_bounded(&bar_dq, 0, g);
         ptx::tc_fence_after();
         __nv_bfloat16 *dst_row = dq + ((size_t)bh * n + (row_ok ? row : 0)) * D;
 #pragma unroll
         for (int c = 0; c < D / 2; c += 32) {
-            const int col = wg * (D / 2) + c;
+            const int col = h * (D / 2) + c;
             uint32_t v[32];
             ptx::tmem_ld32(tmem + lane_off + C::TM_DQ + col, v);
             ptx::tmem_ld_wait();
@@ -1194,7 +1228,7 @@ cudaError_t launch_dq_d(const BwdArgs &a, cudaStream_t stream)
     const int n_qblocks = (a.n + C::BM - 1) / C::BM;
     const long long ctas = (long long)n_qblocks * a.bh;
     bwd_dq_kernel<D><<<(unsigned)ctas, C::THREADS, C::SMEM_BYTES, stream>>>(
-        a.tm_q, a.tm_do, a.tm_k64, a.tm_v64, a.stats,
+        a.tm_q, a.tm_do, a.tm_k, a.tm_v, a.stats,
         reinterpret_cast<__nv_bfloat16 *>(a.dq), a.n, a.n_pad, n_qblocks, a.scale, a.status);
     return cudaGetLastError();
 }

@@ -21,7 +21,6 @@ struct FwdArgs {
 
 struct BwdArgs {
     CUtensorMap tm_q, tm_k, tm_v, tm_do;
-    CUtensorMap tm_k64, tm_v64;     // K and V with 64-row boxes (deterministic dQ pass only)
     CUtensorMap tm_dk, tm_dv;       // dK and dV with 128-row boxes (tile stores, d = 64)
     const void *o, *dout;           // [BH, N, d] bf16
     const float *lse;               // [BH, N]
