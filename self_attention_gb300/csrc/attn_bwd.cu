@@ -510,6 +510,7 @@ struct WideCfg {
     __host__ __device__ static constexpr uint32_t tm_s(int b) { return 256 + b * 128; }
 };
 
+template <bool WITH_DQ>
 __global__ void __launch_bounds__(384, 1)
     bwd_main_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -675,15 +676,18 @@ __global__ void __launch_bounds__(384, 1)
                     ptx::mma_commit(&bar_dp_full);
                 }
                 issue_dv(s, b, it > 0);
-                issue_dq(b);
-                ptx::mma_commit(&bar_dq_full[b]);
+                if constexpr (WITH_DQ) {
+                    issue_dq(b);
+                    ptx::mma_commit(&bar_dq_full[b]);
+                }
                 issue_dk(s, b, it > 0);
                 ptx::mma_commit(&bar_qe[s]);
                 ptx::mma_commit(&bar_ds_empty[b]);
                 if (it + 2 < nq) {
                     const int s2 = (it + 2) % C::QST;
                     wait_bounded(&bar_qf[s2], ((it + 2) / C::QST) & 1, g);
-                    wait_bounded(&bar_dq_empty[b], (it >> 1) & 1, g);   // dQ_i^T drained
+                    if constexpr (WITH_DQ)
+                        wait_bounded(&bar_dq_empty[b], (it >> 1) & 1, g);   // dQ_i^T drained
                     ptx::tc_fence_after();
                     issue_s(s2, b);
                     ptx::mma_commit(&bar_s_full[b]);
@@ -822,7 +826,7 @@ __global__ void __launch_bounds__(384, 1)
                 ptx::bulk_wait_group<0>();   // complete before the CTA exits
             }
         }
-    } else if (warp < 10) {
+    } else if (WITH_DQ && warp < 10) {
         // ---------------------------------------------------------------- dQ warps
         const int r = (warp - 8) * 32 + lane;   // d column = TMEM lane of dQ^T
         const uint32_t lane_off = (uint32_t)((warp - 8) * 32) << 16;
@@ -1199,15 +1203,16 @@ cudaError_t launch_bwd_preprocess(const BwdArgs &a, cudaStream_t stream)
     return a.d == 64 ? launch_preprocess_d<64>(a, true, stream) : launch_preprocess_d<128>(a, true, stream);
 }
 
-static cudaError_t launch_main_wide(const BwdArgs &a, cudaStream_t stream)
+template <bool WITH_DQ>
+cudaError_t launch_main_wide(const BwdArgs &a, cudaStream_t stream)
 {
     using C = WideCfg;
-    cudaError_t e = cudaFuncSetAttribute(bwd_main_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(bwd_main_wide_kernel<WITH_DQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int n_kvblocks = (a.n + C::BN - 1) / C::BN;
     const long long ctas = (long long)n_kvblocks * a.bh;
-    bwd_main_wide_kernel<<<(unsigned)ctas, C::THREADS, C::SMEM_BYTES, stream>>>(
+    bwd_main_wide_kernel<WITH_DQ><<<(unsigned)ctas, C::THREADS, C::SMEM_BYTES, stream>>>(
         a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dk, a.tm_dv, a.stats, a.dq_acc, a.n, a.n_pad, n_kvblocks,
         a.scale, a.status);
     return cudaGetLastError();
@@ -1215,7 +1220,7 @@ static cudaError_t launch_main_wide(const BwdArgs &a, cudaStream_t stream)
 
 cudaError_t launch_bwd_main(const BwdArgs &a, cudaStream_t stream)
 {
-    return a.d == 64 ? launch_main_wide(a, stream) : launch_main_d<128, true>(a, stream);
+    return a.d == 64 ? launch_main_wide<true>(a, stream) : launch_main_d<128, true>(a, stream);
 }
 
 template <int D>
@@ -1238,7 +1243,7 @@ cudaError_t launch_bwd_deterministic(const BwdArgs &a, cudaStream_t stream)
     cudaError_t e = a.d == 64 ? launch_preprocess_d<64>(a, false, stream)
                               : launch_preprocess_d<128>(a, false, stream);
     if (e == cudaSuccess)
-        e = a.d == 64 ? launch_main_d<64, false>(a, stream) : launch_main_d<128, false>(a, stream);
+        e = a.d == 64 ? launch_main_wide<false>(a, stream) : launch_main_d<128, false>(a, stream);
     if (e == cudaSuccess) e = a.d == 64 ? launch_dq_d<64>(a, stream) : launch_dq_d<128>(a, stream);
     return e;
 }
