@@ -878,6 +878,349 @@ __global__ void __launch_bounds__(384, 1)
     }
 }
 
+// ------------------------------------------------------------------ 2''. dK / dV only, d = 128
+// The deterministic mode's dK, dV pass for d = 128 with 128-query tiles, so that its four
+// products run at N = 128 (S^T and dP^T at N = 64 take as long as at N = 128).  TMEM holds dK,
+// dV, dP^T and one S^T buffer (4 x 128 columns).
+//   warp 16     TMA: K_j and V_j once; Q_i (+ its statistics) in two slots, dO_i in one.
+//   warp 17     tcgen05, per query tile i: once P^T is in, dV += P^T dO_i and S^T of tile
+//               i + 1 (over P^T, after dV has read it); once dS^T is in, dK += dS^T Q_i and dP^T
+//               of tile i + 1.
+//   warps 0-15  four warpgroups on the same tile, warpgroup w on its queries [32w, 32w + 32);
+//               thread = key row: P^T (bf16 over the group's S^T columns, fp32 kept), then dS^T
+//               (bf16) into the dS^T tile.  At the end warpgroups 0-1 write dK (times scale) and
+//               2-3 dV, 64 columns each, through the Q slots and TMA stores.
+// TMEM columns: dK [0,128), dV [128,256), dP^T [256,384), S^T [384,512).
+struct D128Cfg {
+    static constexpr int D = 128;
+    static constexpr int BN = 128;   // keys per CTA
+    static constexpr int BM = 128;   // queries per tile
+    static constexpr int QST = 2;    // Q slots
+    static constexpr int T_BYTES = 128 * D * 2;       // one 128 x 128 bf16 tile, two 64-column blocks
+    static constexpr int BLK = 128 * 128;             // bytes of one 64-column block of 128 rows
+    static constexpr int LD_BYTES = 2 * BM * 4;       // statistics of one tile
+    static constexpr int SMEM_BYTES = 2 * T_BYTES + QST * T_BYTES + T_BYTES + T_BYTES + QST * LD_BYTES + 1024;
+    static constexpr int PDS_WARPS = 16;
+    static constexpr int THREADS = 32 * (PDS_WARPS + 2);
+    static constexpr int TMA_WARP = PDS_WARPS, MMA_WARP = PDS_WARPS + 1;
+    static constexpr uint32_t TM_DK = 0, TM_DV = 128, TM_DP = 256, TM_S = 384;
+};
+
+__global__ void __launch_bounds__(D128Cfg::THREADS, 1)
+    bwd_dkdv_d128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                         const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
+                         const float *__restrict__ stats, int n, int n_pad, int n_kvblocks, float scale,
+                         int *status)
+{
+    using C = D128Cfg;
+    constexpr int D = C::D;
+    constexpr uint32_t PDS_THREADS = 32 * C::PDS_WARPS;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    uint8_t *sK = smem;
+    uint8_t *sV = sK + C::T_BYTES;
+    uint8_t *sQ = sV + C::T_BYTES;                  // QST slots of Q_i
+    uint8_t *sDO = sQ + C::QST * C::T_BYTES;        // dO_i
+    uint8_t *sDS = sDO + C::T_BYTES;                // dS^T, two 64-query blocks of 128 key rows
+    float *sLD = reinterpret_cast<float *>(sDS + C::T_BYTES);   // QST x statistics
+
+    __shared__ uint64_t bar_kv, bar_qf[C::QST], bar_qe[C::QST], bar_dof, bar_doe;
+    __shared__ uint64_t bar_s_full, bar_p_full, bar_dp_full, bar_ds_full, bar_dkv, bar_done;
+    __shared__ uint32_t tmem_sh;
+    __shared__ int abort_sh;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.x / n_kvblocks;
+    const int kv0 = (blockIdx.x % n_kvblocks) * C::BN;
+    const int nq = (n + C::BM - 1) / C::BM;
+    const Guard g{&abort_sh, status, kWaitLimitNs};
+
+    if (threadIdx.x == 0) {
+        abort_sh = 0;
+        ptx::mbar_init(&bar_kv, 1);
+        for (int s = 0; s < C::QST; ++s) {
+            ptx::mbar_init(&bar_qf[s], 1);
+            ptx::mbar_init(&bar_qe[s], 1);
+        }
+        ptx::mbar_init(&bar_dof, 1);
+        ptx::mbar_init(&bar_doe, 1);
+        ptx::mbar_init(&bar_s_full, 1);
+        ptx::mbar_init(&bar_p_full, PDS_THREADS);
+        ptx::mbar_init(&bar_dp_full, 1);
+        ptx::mbar_init(&bar_ds_full, PDS_THREADS);
+        ptx::mbar_init(&bar_dkv, 1);
+        ptx::mbar_init(&bar_done, 1);
+        ptx::fence_mbar_init();
+    }
+    if (warp == C::MMA_WARP) {
+        ptx::tmem_alloc(&tmem_sh, 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = tmem_sh;
+
+    if (warp == C::TMA_WARP) {
+        // ---------------------------------------------------------------- TMA producer
+        if (ptx::elect_one()) {
+            ptx::tma_prefetch_desc(&tm_q);
+            ptx::tma_prefetch_desc(&tm_k);
+            ptx::tma_prefetch_desc(&tm_v);
+            ptx::tma_prefetch_desc(&tm_do);
+            ptx::mbar_arrive_expect_tx(&bar_kv, 2 * C::T_BYTES);
+            for (int h = 0; h < 2; ++h) {
+                ptx::tma_load_3d(sK + h * C::BLK, &tm_k, &bar_kv, h * 64, kv0, bh);
+                ptx::tma_load_3d(sV + h * C::BLK, &tm_v, &bar_kv, h * 64, kv0, bh);
+            }
+            // The Q / dO maps have 64-row boxes: four per tile (two column blocks x two row
+            // halves), contiguous in the 128-byte-swizzled layout of each column block.
+            for (int it = 0; it < nq; ++it) {
+                const int s = it & 1;
+                wait_bounded(&bar_qe[s], ((it >> 1) & 1) ^ 1, g);
+                ptx::mbar_arrive_expect_tx(&bar_qf[s], C::T_BYTES + C::LD_BYTES);
+                uint8_t *slot = sQ + s * C::T_BYTES;
+                for (int h = 0; h < 2; ++h)
+                    for (int rr = 0; rr < 2; ++rr)
+                        ptx::tma_load_3d(slot + h * C::BLK + rr * 64 * 128, &tm_q, &bar_qf[s], h * 64,
+                                         it * C::BM + rr * 64, bh);
+                const size_t rowvec = (size_t)bh * n_pad + (size_t)it * C::BM;
+                ptx::bulk_load(sLD + s * 2 * C::BM, stats + rowvec * 2, C::BM * 8, &bar_qf[s]);
+                wait_bounded(&bar_doe, (it & 1) ^ 1, g);
+                ptx::mbar_arrive_expect_tx(&bar_dof, C::T_BYTES);
+                for (int h = 0; h < 2; ++h)
+                    for (int rr = 0; rr < 2; ++rr)
+                        ptx::tma_load_3d(sDO + h * C::BLK + rr * 64 * 128, &tm_do, &bar_dof, h * 64,
+                                         it * C::BM + rr * 64, bh);
+            }
+            wait_bounded(&bar_kv, 0, g);
+            for (int it = (nq > C::QST ? nq - C::QST : 0); it < nq; ++it)
+                wait_bounded(&bar_qf[it & 1], (it >> 1) & 1, g);
+            if (nq > 0) wait_bounded(&bar_dof, (nq - 1) & 1, g);
+        }
+    } else if (warp == C::MMA_WARP) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (ptx::elect_one()) {
+            const uint32_t idSdP = ptx::idesc_bf16_f32(128, C::BM, false, false);
+            const uint32_t idKV = ptx::idesc_bf16_f32(128, D, false, true);
+            const uint32_t k_base = ptx::smem_u32(sK), v_base = ptx::smem_u32(sV);
+            const uint32_t q_base = ptx::smem_u32(sQ), do_base = ptx::smem_u32(sDO);
+            const uint32_t ds_base = ptx::smem_u32(sDS);
+            // S^T = K_j Q_i^T and dP^T = V_j dO_i^T: all four operands K-major over d (two
+            // 64-column blocks), N = 128 queries.
+            auto issue_s = [&](int s) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * C::BLK + (kk & 3) * 32;
+                    ptx::mma_ss(tmem + C::TM_S, ptx::sdesc_sw128(k_base + off, 16, 1024),
+                                ptx::sdesc_sw128(q_base + s * C::T_BYTES + off, 16, 1024), idSdP, kk > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_dp = [&]() {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * C::BLK + (kk & 3) * 32;
+                    ptx::mma_ss(tmem + C::TM_DP, ptx::sdesc_sw128(v_base + off, 16, 1024),
+                                ptx::sdesc_sw128(do_base + off, 16, 1024), idSdP, kk > 0 ? 1u : 0u);
+                }
+            };
+            // dV += P^T dO_i: P^T of queries [16kk, 16kk + 16) sits in the S^T columns of the
+            // warpgroup that produced it (32 (kk / 2) + 8 (kk % 2)); dO_i MN-major (N = d in two
+            // 64-column blocks BLK bytes apart).
+            auto issue_dv = [&](bool acc) {
+#pragma unroll
+                for (int kk = 0; kk < C::BM / 16; ++kk)
+                    ptx::mma_ts(tmem + C::TM_DV, tmem + C::TM_S + (kk >> 1) * 32 + (kk & 1) * 8,
+                                ptx::sdesc_sw128(do_base + kk * 2048, C::BLK, 1024), idKV,
+                                (acc || kk > 0) ? 1u : 0u);
+            };
+            // dK += dS^T Q_i: dS^T K-major (two 64-query blocks BLK bytes apart), Q_i MN-major.
+            auto issue_dk = [&](int s, bool acc) {
+#pragma unroll
+                for (int kk = 0; kk < C::BM / 16; ++kk)
+                    ptx::mma_ss(tmem + C::TM_DK,
+                                ptx::sdesc_sw128(ds_base + (kk >> 2) * C::BLK + (kk & 3) * 32, 16, 1024),
+                                ptx::sdesc_sw128(q_base + s * C::T_BYTES + kk * 2048, C::BLK, 1024), idKV,
+                                (acc || kk > 0) ? 1u : 0u);
+            };
+            wait_bounded(&bar_kv, 0, g);
+            if (nq > 0) {
+                wait_bounded(&bar_qf[0], 0, g);
+                ptx::tc_fence_after();
+                issue_s(0);
+                ptx::mma_commit(&bar_s_full);
+                wait_bounded(&bar_dof, 0, g);
+                ptx::tc_fence_after();
+                issue_dp();
+                ptx::mma_commit(&bar_dp_full);
+            }
+            for (int it = 0; it < nq; ++it) {
+                const int s = it & 1;
+                const bool more = it + 1 < nq;
+                wait_bounded(&bar_p_full, it & 1, g);
+                ptx::tc_fence_after();
+                issue_dv(it > 0);
+                ptx::mma_commit(&bar_doe);                     // dO_i read (dP^T and dV)
+                if (more) {   // over P^T, after dV has read it (in order)
+                    wait_bounded(&bar_qf[s ^ 1], ((it + 1) >> 1) & 1, g);
+                    ptx::tc_fence_after();
+                    issue_s(s ^ 1);
+                    ptx::mma_commit(&bar_s_full);
+                }
+                wait_bounded(&bar_ds_full, it & 1, g);
+                ptx::tc_fence_after();
+                issue_dk(s, it > 0);
+                ptx::mma_commit(&bar_qe[s]);
+                if (more) {   // dP^T is free: the P / dS warps have read it (dS^T is in)
+                    wait_bounded(&bar_dof, (it + 1) & 1, g);
+                    ptx::tc_fence_after();
+                    issue_dp();
+                    ptx::mma_commit(&bar_dp_full);
+                }
+            }
+            ptx::mma_commit(&bar_dkv);
+            ptx::mma_commit(&bar_done);
+            wait_bounded(&bar_done, 0, g);
+        }
+    } else {
+        // ---------------------------------------------------------------- P / dS warpgroups
+        const int wg = warp >> 2, cw = warp & 3;
+        const int r = cw * 32 + lane;       // key row within the tile = TMEM lane
+        const bool key_ok = kv0 + r < n;
+        const uint32_t lane_off = (uint32_t)(cw * 32) << 16;
+        const float scale_log2 = scale * kLog2e;
+        const uint64_t c2 = ptx::f2_pack(scale_log2, scale_log2);
+        const uint32_t rowp_a = ptx::smem_u32(sDS + (wg >> 1) * C::BLK + r * 128);
+        const int chunk0 = (wg & 1) * 4;    // the group's 32 queries: 16-byte chunks [chunk0, chunk0 + 4)
+        const uint32_t tS = tmem + lane_off + C::TM_S + wg * 32;
+        const uint32_t tDP = tmem + lane_off + C::TM_DP + wg * 32;
+        for (int it = 0; it < nq; ++it) {
+            const int s = it & 1;
+            // {-LSE2 pair, -D pair} per two of this warpgroup's queries
+            const uint32_t sst_a = ptx::smem_u32(sLD + s * 2 * C::BM + wg * 64);
+            wait_bounded(&bar_s_full, it & 1, g);
+            ptx::tc_fence_after();
+            // Phase 1, as soon as S^T is in: P^T = 2^(S^T c - LSE2), 16 queries at a time (the
+            // next 16 columns load meanwhile), bf16 back into TMEM over S^T columns already
+            // read, fp32 kept for dS.
+            float pf[32];
+            {
+                uint32_t sv[2][16];
+                ptx::tmem_ld16(tS, sv[0]);
+                ptx::tmem_ld16(tS + 16, sv[1]);
+                ptx::tmem_ld_wait();
+                reg_fence(sv[0]);
+                reg_fence(sv[1]);
+#pragma unroll
+                for (int qt = 0; qt < 2; ++qt) {
+                    uint2 nl[8];   // -LSE2 of queries (c, c + 1), c = 0, 2, ..., 14
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) nl[e] = lds_u64(sst_a + (qt * 16 + 2 * e) * 8);
+                    uint32_t pp[8];
+#pragma unroll
+                    for (int c = 0; c < 16; c += 2) {
+                        const uint64_t x = ptx::fma_f32x2(
+                            ptx::f2_pack(__uint_as_float(sv[qt][c]), __uint_as_float(sv[qt][c + 1])), c2,
+                            ((uint64_t)nl[c / 2].y << 32) | nl[c / 2].x);
+                        float x0, x1;
+                        ptx::f2_unpack(x, x0, x1);
+                        float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+                        if (!key_ok) p0 = p1 = 0.f;
+                        pf[qt * 16 + c] = p0;
+                        pf[qt * 16 + c + 1] = p1;
+                        pp[c / 2] = ptx::pack_bf16x2(p0, p1);
+                    }
+                    ptx::tmem_st8(tS + qt * 8, pp);
+                }
+            }
+            ptx::tmem_st_wait();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&bar_p_full);
+            // Phase 2, once dP^T is in (which also means tile i - 1's dK, issued before it, is
+            // done with the dS^T tile): dS^T = P^T o (dP^T - D), bf16 into shared memory.
+            wait_bounded(&bar_dp_full, it & 1, g);
+            ptx::tc_fence_after();
+            {
+                uint32_t dpv[2][16];
+                ptx::tmem_ld16(tDP, dpv[0]);
+                ptx::tmem_ld16(tDP + 16, dpv[1]);
+                ptx::tmem_ld_wait();
+                reg_fence(dpv[0]);
+                reg_fence(dpv[1]);
+#pragma unroll
+                for (int qt = 0; qt < 2; ++qt) {
+                    uint2 nd[8];   // -D of queries (c, c + 1)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) nd[e] = lds_u64(sst_a + (qt * 16 + 2 * e) * 8 + 8);
+                    uint32_t dsp[8];
+#pragma unroll
+                    for (int c = 0; c < 16; c += 2) {
+                        const uint64_t dsq = ptx::mul_f32x2(
+                            ptx::f2_pack(pf[qt * 16 + c], pf[qt * 16 + c + 1]),
+                            ptx::add_f32x2(ptx::f2_pack(__uint_as_float(dpv[qt][c]), __uint_as_float(dpv[qt][c + 1])),
+                                           ((uint64_t)nd[c / 2].y << 32) | nd[c / 2].x));
+                        float ds0, ds1;
+                        ptx::f2_unpack(dsq, ds0, ds1);
+                        dsp[c / 2] = ptx::pack_bf16x2(ds0, ds1);
+                    }
+#pragma unroll
+                    for (int cc = 0; cc < 2; ++cc)
+                        sts_u128(rowp_a + (((chunk0 + qt * 2 + cc) ^ (r & 7)) << 4),
+                                 make_uint4(dsp[4 * cc], dsp[4 * cc + 1], dsp[4 * cc + 2], dsp[4 * cc + 3]));
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&bar_ds_full);
+        }
+        // epilogue: warpgroups 0-1 write dK = scale * acc, 2-3 dV = acc, 64 columns each, bf16,
+        // staged in the now idle Q slots in the 128-byte-swizzled layout (16-byte chunk c of
+        // row r at chunk c ^ (r % 8), one 64-column block per group) and stored with TMA tensor
+        // stores (rows past N clipped)
+        wait_bounded(&bar_dkv, 0, g);
+        ptx::tc_fence_after();
+        {
+            const int which = wg >> 1, half = wg & 1;
+            const float mul = which == 0 ? scale : 1.f;
+            const uint32_t col0 = (which == 0 ? C::TM_DK : C::TM_DV) + half * 64;
+            const uint32_t srow = ptx::smem_u32(sQ + which * C::T_BYTES + half * C::BLK) + r * 128;
+#pragma unroll
+            for (int c = 0; c < 64; c += 32) {
+                uint32_t v[32];
+                ptx::tmem_ld32(tmem + lane_off + col0 + c, v);
+                ptx::tmem_ld_wait();
+                reg_fence(v);
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    pk[e] = ptx::pack_bf16x2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+#pragma unroll
+                for (int v4 = 0; v4 < 4; ++v4)
+                    sts_u128(srow + ((((c >> 3) + v4) ^ (r & 7)) << 4),
+                             make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]));
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::named_bar(1, PDS_THREADS);
+            if (threadIdx.x == 0) {
+                for (int h = 0; h < 2; ++h) {
+                    ptx::tma_store_3d(&tm_dk, sQ + h * C::BLK, h * 64, kv0, bh);
+                    ptx::tma_store_3d(&tm_dv, sQ + C::T_BYTES + h * C::BLK, h * 64, kv0, bh);
+                }
+                ptx::bulk_commit_group();
+                ptx::bulk_wait_group<0>();   // complete before the CTA exits
+            }
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == C::MMA_WARP) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 512);
+    }
+}
+
 // ------------------------------------------------------------------ 4. deterministic dQ pass
 // dQ_i = scale * sum_j dS_ij K_j without atomics: one CTA owns 128 query rows of one head and
 // walks the key tiles (128 keys each) in order, recomputing S = Q K^T and dP = dO V^T on chip.
@@ -1218,6 +1561,20 @@ cudaError_t launch_main_wide(const BwdArgs &a, cudaStream_t stream)
     return cudaGetLastError();
 }
 
+cudaError_t launch_dkdv_d128(const BwdArgs &a, cudaStream_t stream)
+{
+    using C = D128Cfg;
+    cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_d128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int n_kvblocks = (a.n + C::BN - 1) / C::BN;
+    const long long ctas = (long long)n_kvblocks * a.bh;
+    bwd_dkdv_d128_kernel<<<(unsigned)ctas, C::THREADS, C::SMEM_BYTES, stream>>>(
+        a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dk, a.tm_dv, a.stats, a.n, a.n_pad, n_kvblocks, a.scale,
+        a.status);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_bwd_main(const BwdArgs &a, cudaStream_t stream)
 {
     return a.d == 64 ? launch_main_wide<true>(a, stream) : launch_main_d<128, true>(a, stream);
@@ -1243,7 +1600,7 @@ cudaError_t launch_bwd_deterministic(const BwdArgs &a, cudaStream_t stream)
     cudaError_t e = a.d == 64 ? launch_preprocess_d<64>(a, false, stream)
                               : launch_preprocess_d<128>(a, false, stream);
     if (e == cudaSuccess)
-        e = a.d == 64 ? launch_main_wide<false>(a, stream) : launch_main_d<128, false>(a, stream);
+        e = a.d == 64 ? launch_main_wide<false>(a, stream) : launch_dkdv_d128(a, stream);
     if (e == cudaSuccess) e = a.d == 64 ? launch_dq_d<64>(a, stream) : launch_dq_d<128>(a, stream);
     return e;
 }
