@@ -36,6 +36,8 @@ namespace attn {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
+// Longest sequence for which the d = 64 backward runs as a persistent kernel.
+constexpr int kBwdPersistentMaxN = 4096;
 
 template <int D>
 struct BwdCfg {
@@ -878,6 +880,513 @@ __global__ void __launch_bounds__(384, 1)
     }
 }
 
+// ------------------------------------------------------------------ 2'''. main, d = 64, persistent
+// For short sequences (few query tiles per key block) the wide kernel's fixed costs per CTA
+// (start-up loads, the dK / dV epilogue, the last dQ reduce-adds) are as long as its products.
+// This variant keeps one CTA per SM and runs its (head, key block) items as one sequence of
+// query tiles, so that the tile pipeline's lookahead (dP^T one tile, S^T two tiles ahead)
+// crosses item boundaries and the next item's loads and products overlap the previous item's
+// tail.
+//   warp 10     TMA: per item K into one of two buffers and V into one buffer (free once the
+//               previous item's last dP^T has read it); per tile Q (+ statistics) through a
+//               ring of three and dO through a ring of two.
+//   warp 11     tcgen05, per tile t of the sequence, as the wide kernel; dK and dV restart
+//               (accumulate off) on the first tile of each item.
+//   warps 0-7   P / dS as the wide kernel; after the P phase of an item's first tile, the
+//               previous item's dK (warpgroup 0, times scale) and dV (warpgroup 1) go from
+//               TMEM through the idle dS^T buffer (the previous tile's, whose products are
+//               done) to global memory by TMA tensor stores.
+//   warps 8-9   dQ drain as the wide kernel (32 query rows per staged chunk; 16-row chunks,
+//               which would leave room for a third dO buffer, drain ~1.3x slower).
+// TMEM columns as the wide kernel.  Items (head, key block) are taken in a grid-stride order.
+struct PersistBwdCfg {
+    static constexpr int D = 64;
+    static constexpr int BN = 128, BM = 128;
+    static constexpr int QST = 3, DOST = 2;
+    static constexpr int T_BYTES = 128 * D * 2;        // one 128-row tile
+    static constexpr int LD_BYTES = 2 * BM * 4;
+    static constexpr int DS_BYTES = BN * BM * 2;       // two 64-query blocks of BN rows
+    static constexpr int DQC_ROWS = 32;
+    static constexpr int DQC_BYTES = DQC_ROWS * D * 4; // dQ staging: 32 query rows
+    static constexpr int SMEM_BYTES = 3 * T_BYTES + QST * T_BYTES + DOST * T_BYTES + 2 * DS_BYTES +
+                                      2 * DQC_BYTES + QST * LD_BYTES + 1024;
+    static constexpr int THREADS = 384;
+    static constexpr int TMA_WARP = 10, MMA_WARP = 11;
+    static constexpr uint32_t TM_DK = 0, TM_DV = 64, TM_DP = 128;
+    __host__ __device__ static constexpr uint32_t tm_s(int b) { return 256 + b * 128; }
+};
+
+// Position of tile t of a CTA's sequence: item li (head bh, keys from kv0), query tile it.
+struct TileCursor {
+    int li, it, bh, kv0;
+    __device__ void start(int first, int n_kvblocks, int bn)
+    {
+        li = 0;
+        it = 0;
+        bh = first / n_kvblocks;
+        kv0 = (first % n_kvblocks) * bn;
+    }
+    __device__ void next(int nq, int first, int stride, int n_kvblocks, int bn)
+    {
+        if (++it == nq) {
+            it = 0;
+            ++li;
+            const int item = first + li * stride;
+            bh = item / n_kvblocks;
+            kv0 = (item % n_kvblocks) * bn;
+        }
+    }
+};
+
+template <bool WITH_DQ>
+__global__ void __launch_bounds__(384, 1)
+    bwd_main_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                            const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
+                            const float *__restrict__ stats, float *__restrict__ dq_acc, int n, int n_pad,
+                            int n_kvblocks, int n_items, float scale, int *status)
+{
+    using C = PersistBwdCfg;
+    constexpr int D = C::D;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    uint8_t *sK = smem;                             // K_0, K_1, then V (dQ^T's unused rows read on)
+    uint8_t *sV = sK + 2 * C::T_BYTES;
+    uint8_t *sQ = sV + C::T_BYTES;                  // QST Q tiles
+    uint8_t *sDO = sQ + C::QST * C::T_BYTES;        // DOST dO tiles
+    uint8_t *sDS = sDO + C::DOST * C::T_BYTES;      // two dS^T tiles
+    float *sDQ = reinterpret_cast<float *>(sDS + 2 * C::DS_BYTES);                       // 2 x [32][D]
+    float *sLD = reinterpret_cast<float *>(sDS + 2 * C::DS_BYTES + 2 * C::DQC_BYTES);   // QST x stats
+
+    __shared__ uint64_t bar_kf[2], bar_ke[2], bar_vf, bar_ve, bar_qf[C::QST], bar_qe[C::QST];
+    __shared__ uint64_t bar_dof[C::DOST], bar_doe[C::DOST];
+    __shared__ uint64_t bar_s_full[2], bar_dp_full, bar_ds_full, bar_ds_empty[2], bar_dq_full[2], bar_dq_empty[2];
+    __shared__ uint64_t bar_dkv, bar_done;
+    __shared__ uint32_t tmem_sh;
+    __shared__ int abort_sh;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nq = (n + C::BM - 1) / C::BM;
+    const int first = blockIdx.x, stride = gridDim.x;
+    const int n_mine = first < n_items ? (n_items - 1 - first) / stride + 1 : 0;
+    const int T = n_mine * nq;                      // query tiles in this CTA's sequence
+    const Guard g{&abort_sh, status, kWaitLimitNs};
+
+    if (threadIdx.x == 0) {
+        abort_sh = 0;
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(&bar_kf[b], 1);
+            ptx::mbar_init(&bar_ke[b], 1);
+            ptx::mbar_init(&bar_s_full[b], 1);
+            ptx::mbar_init(&bar_ds_empty[b], 1);
+            ptx::mbar_init(&bar_dq_full[b], 1);
+            ptx::mbar_init(&bar_dq_empty[b], 64);
+        }
+        ptx::mbar_init(&bar_vf, 1);
+        ptx::mbar_init(&bar_ve, 1);
+        for (int s = 0; s < C::QST; ++s) {
+            ptx::mbar_init(&bar_qf[s], 1);
+            ptx::mbar_init(&bar_qe[s], 1);
+        }
+        for (int s = 0; s < C::DOST; ++s) {
+            ptx::mbar_init(&bar_dof[s], 1);
+            ptx::mbar_init(&bar_doe[s], 1);
+        }
+        ptx::mbar_init(&bar_dp_full, 1);
+        ptx::mbar_init(&bar_ds_full, 256);
+        ptx::mbar_init(&bar_dkv, 1);
+        ptx::mbar_init(&bar_done, 1);
+        ptx::fence_mbar_init();
+    }
+    if (warp == C::MMA_WARP) {
+        ptx::tmem_alloc(&tmem_sh, 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = tmem_sh;
+
+    if (warp == C::TMA_WARP) {
+        // ---------------------------------------------------------------- TMA producer
+        if (ptx::elect_one()) {
+            ptx::tma_prefetch_desc(&tm_q);
+            ptx::tma_prefetch_desc(&tm_k);
+            ptx::tma_prefetch_desc(&tm_v);
+            ptx::tma_prefetch_desc(&tm_do);
+            TileCursor c;
+            c.start(first, n_kvblocks, C::BN);
+            for (int t = 0; t < T; ++t) {
+                if (c.it == 0) {   // K into buffer li % 2, once item li - 2 is done with it
+                    const int kb = c.li & 1;
+                    wait_bounded(&bar_ke[kb], ((c.li >> 1) & 1) ^ 1, g);
+                    ptx::mbar_arrive_expect_tx(&bar_kf[kb], C::T_BYTES);
+                    ptx::tma_load_3d(sK + kb * C::T_BYTES, &tm_k, &bar_kf[kb], 0, c.kv0, c.bh);
+                }
+                const int s = t % C::QST;
+                wait_bounded(&bar_qe[s], ((t / C::QST) & 1) ^ 1, g);
+                ptx::mbar_arrive_expect_tx(&bar_qf[s], C::T_BYTES + C::LD_BYTES);
+                // the Q / dO maps have 64-row boxes: two per 128-row tile, contiguous in the
+                // 128-byte-swizzled layout
+                for (int h = 0; h < 2; ++h)
+                    ptx::tma_load_3d(sQ + s * C::T_BYTES + h * 64 * 128, &tm_q, &bar_qf[s], 0,
+                                     c.it * C::BM + h * 64, c.bh);
+                const size_t rowvec = (size_t)c.bh * n_pad + (size_t)c.it * C::BM;
+                ptx::bulk_load(sLD + s * 2 * C::BM, stats + rowvec * 2, C::BM * 8, &bar_qf[s]);
+                if (c.it == 0) {   // V, once the previous item's last dP^T has read it
+                    wait_bounded(&bar_ve, (c.li & 1) ^ 1, g);
+                    ptx::mbar_arrive_expect_tx(&bar_vf, C::T_BYTES);
+                    ptx::tma_load_3d(sV, &tm_v, &bar_vf, 0, c.kv0, c.bh);
+                }
+                const int sd = t % C::DOST;
+                wait_bounded(&bar_doe[sd], ((t / C::DOST) & 1) ^ 1, g);
+                ptx::mbar_arrive_expect_tx(&bar_dof[sd], C::T_BYTES);
+                for (int h = 0; h < 2; ++h)
+                    ptx::tma_load_3d(sDO + sd * C::T_BYTES + h * 64 * 128, &tm_do, &bar_dof[sd], 0,
+                                     c.it * C::BM + h * 64, c.bh);
+                c.next(nq, first, stride, n_kvblocks, C::BN);
+            }
+            // Do not leave the CTA with copies in flight (matters only after a timeout).
+            for (int t = (T > C::QST ? T - C::QST : 0); t < T; ++t) wait_bounded(&bar_qf[t % C::QST], (t / C::QST) & 1, g);
+            for (int t = (T > C::DOST ? T - C::DOST : 0); t < T; ++t)
+                wait_bounded(&bar_dof[t % C::DOST], (t / C::DOST) & 1, g);
+            for (int li = (n_mine > 2 ? n_mine - 2 : 0); li < n_mine; ++li)
+                wait_bounded(&bar_kf[li & 1], (li >> 1) & 1, g);
+            if (n_mine > 0) wait_bounded(&bar_vf, (n_mine - 1) & 1, g);
+        }
+    } else if (warp == C::MMA_WARP) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (ptx::elect_one()) {
+            const uint32_t idSdP = ptx::idesc_bf16_f32(128, C::BM, false, false);
+            const uint32_t idKV = ptx::idesc_bf16_f32(128, D, false, true);
+            const uint32_t idDQ = ptx::idesc_bf16_f32(128, C::BM, true, true);
+            const uint32_t k_base = ptx::smem_u32(sK), v_base = ptx::smem_u32(sV);
+            const uint32_t q_base = ptx::smem_u32(sQ), do_base = ptx::smem_u32(sDO);
+            const uint32_t ds_base = ptx::smem_u32(sDS);
+            // S^T = K Q_t^T and dP^T = V dO_t^T: K-major over d, N = 128 query rows.
+            auto issue_s = [&](int kb, int s, int b) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    ptx::mma_ss(tmem + C::tm_s(b), ptx::sdesc_sw128(k_base + kb * C::T_BYTES + kk * 32, 16, 1024),
+                                ptx::sdesc_sw128(q_base + s * C::T_BYTES + kk * 32, 16, 1024), idSdP, kk > 0 ? 1u : 0u);
+            };
+            auto issue_dp = [&](int sd) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    ptx::mma_ss(tmem + C::TM_DP, ptx::sdesc_sw128(v_base + kk * 32, 16, 1024),
+                                ptx::sdesc_sw128(do_base + sd * C::T_BYTES + kk * 32, 16, 1024), idSdP,
+                                kk > 0 ? 1u : 0u);
+            };
+            // dV += P^T dO_t: P^T of queries [16kk, 16kk + 16) in the S^T columns of the
+            // warpgroup that produced it (64 (kk / 4) + 8 (kk % 4)); dO_t MN-major.
+            auto issue_dv = [&](int sd, int b, bool acc) {
+#pragma unroll
+                for (int kk = 0; kk < C::BM / 16; ++kk)
+                    ptx::mma_ts(tmem + C::TM_DV, tmem + C::tm_s(b) + (kk >> 2) * 64 + (kk & 3) * 8,
+                                ptx::sdesc_sw128(do_base + sd * C::T_BYTES + kk * 2048, C::BM * 128, 1024), idKV,
+                                (acc || kk > 0) ? 1u : 0u);
+            };
+            // dK += dS^T Q_t: dS^T K-major (two 64-query blocks BN * 128 bytes apart), Q_t MN-major.
+            auto issue_dk = [&](int s, int b, bool acc) {
+#pragma unroll
+                for (int kk = 0; kk < C::BM / 16; ++kk)
+                    ptx::mma_ss(tmem + C::TM_DK,
+                                ptx::sdesc_sw128(ds_base + b * C::DS_BYTES + (kk >> 2) * (C::BN * 128) + (kk & 3) * 32,
+                                                 16, 1024),
+                                ptx::sdesc_sw128(q_base + s * C::T_BYTES + kk * 2048, C::BM * 128, 1024), idKV,
+                                (acc || kk > 0) ? 1u : 0u);
+            };
+            // dQ_t^T = K^T dS^T over S^T / P^T of tile t: A = K MN-major with M = 128 (rows
+            // 64-127 read the next 16 KB of shared memory and land in unused lanes), B = dS^T
+            // MN-major, N = 128 queries in two blocks BN * 128 bytes apart.
+            auto issue_dq = [&](int kb, int b) {
+#pragma unroll
+                for (int kk = 0; kk < C::BN / 16; ++kk)
+                    ptx::mma_ss(tmem + C::tm_s(b), ptx::sdesc_sw128(k_base + kb * C::T_BYTES + kk * 2048, C::T_BYTES, 1024),
+                                ptx::sdesc_sw128(ds_base + b * C::DS_BYTES + kk * 2048, C::BN * 128, 1024),
+                                idDQ, kk > 0 ? 1u : 0u);
+            };
+            TileCursor c0, c1, c2;   // tiles t, t + 1, t + 2
+            c0.start(first, n_kvblocks, C::BN);
+            c1 = c0;
+            c1.next(nq, first, stride, n_kvblocks, C::BN);
+            c2 = c1;
+            c2.next(nq, first, stride, n_kvblocks, C::BN);
+            if (T > 0) {
+                wait_bounded(&bar_kf[0], 0, g);
+                wait_bounded(&bar_qf[0], 0, g);
+                ptx::tc_fence_after();
+                issue_s(0, 0, 0);
+                ptx::mma_commit(&bar_s_full[0]);
+                wait_bounded(&bar_vf, 0, g);
+                wait_bounded(&bar_dof[0], 0, g);
+                ptx::tc_fence_after();
+                issue_dp(0);
+                ptx::mma_commit(&bar_dp_full);
+                if (nq == 1) ptx::mma_commit(&bar_ve);
+            }
+            if (T > 1) {
+                if (c1.it == 0) wait_bounded(&bar_kf[c1.li & 1], (c1.li >> 1) & 1, g);
+                wait_bounded(&bar_qf[1], 0, g);
+                ptx::tc_fence_after();
+                issue_s(c1.li & 1, 1, 1);
+                ptx::mma_commit(&bar_s_full[1]);
+            }
+            for (int t = 0; t < T; ++t) {
+                const int b = t & 1, s = t % C::QST, sd = t % C::DOST, kb = c0.li & 1;
+                wait_bounded(&bar_ds_full, t & 1, g);
+                ptx::tc_fence_after();
+                if (t + 1 < T) {
+                    if (c1.it == 0) wait_bounded(&bar_vf, c1.li & 1, g);   // the next item's V
+                    wait_bounded(&bar_dof[(t + 1) % C::DOST], ((t + 1) / C::DOST) & 1, g);
+                    ptx::tc_fence_after();
+                    issue_dp((t + 1) % C::DOST);
+                    ptx::mma_commit(&bar_dp_full);
+                    if (c1.it == nq - 1) ptx::mma_commit(&bar_ve);          // its item's last read of V
+                }
+                issue_dv(sd, b, c0.it > 0);
+                ptx::mma_commit(&bar_doe[sd]);
+                if constexpr (WITH_DQ) {
+                    issue_dq(kb, b);
+                    ptx::mma_commit(&bar_dq_full[b]);
+                }
+                issue_dk(s, b, c0.it > 0);
+                ptx::mma_commit(&bar_qe[s]);
+                ptx::mma_commit(&bar_ds_empty[b]);
+                if (c0.it == nq - 1) {   // the item's last products: K free, dK / dV complete
+                    ptx::mma_commit(&bar_ke[kb]);
+                    ptx::mma_commit(&bar_dkv);
+                }
+                if (t + 2 < T) {
+                    const int s2 = (t + 2) % C::QST;
+                    if (c2.it == 0) wait_bounded(&bar_kf[c2.li & 1], (c2.li >> 1) & 1, g);
+                    wait_bounded(&bar_qf[s2], ((t + 2) / C::QST) & 1, g);
+                    if constexpr (WITH_DQ)
+                        wait_bounded(&bar_dq_empty[b], (t >> 1) & 1, g);   // dQ_t^T drained
+                    ptx::tc_fence_after();
+                    issue_s(c2.li & 1, s2, b);
+                    ptx::mma_commit(&bar_s_full[b]);
+                }
+                c0 = c1;
+                c1 = c2;
+                c2.next(nq, first, stride, n_kvblocks, C::BN);
+            }
+            ptx::mma_commit(&bar_done);
+            wait_bounded(&bar_done, 0, g);
+        }
+    } else if (warp < 8) {
+        // ---------------------------------------------------------------- P / dS warpgroups
+        const int wg = warp >> 2, cw = warp & 3;
+        const int r = cw * 32 + lane;       // key row within the tile = TMEM lane
+        const uint32_t lane_off = (uint32_t)(cw * 32) << 16;
+        const float scale_log2 = scale * kLog2e;
+        const uint64_t c2 = ptx::f2_pack(scale_log2, scale_log2);
+        // dK = scale * acc (warpgroup 0) or dV = acc (warpgroup 1) of an item, bf16, into the
+        // 32 KB staging area `stage` (dK then dV, 128-byte-swizzled rows: 16-byte chunk c of row
+        // r at chunk c ^ (r % 8)), then one TMA tensor store each (rows past N clipped).  The
+        // stores still read `stage` afterwards: `store_pending` says so to the caller.
+        bool store_pending = false;
+        auto epilogue = [&](int li, int bh, int kv0, uint8_t *stage) {
+            if (store_pending) {   // earlier stores may still read either buffer
+                if (threadIdx.x == 0) ptx::bulk_wait_group_read<0>();
+                ptx::named_bar(1, 256);
+            }
+            wait_bounded(&bar_dkv, li & 1, g);
+            ptx::tc_fence_after();
+            const float mul = wg == 0 ? scale : 1.f;
+            const uint32_t col0 = wg == 0 ? C::TM_DK : C::TM_DV;
+            const uint32_t srow = ptx::smem_u32(stage + wg * C::T_BYTES) + r * 128;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t v[32];
+                ptx::tmem_ld32(tmem + lane_off + col0 + h * 32, v);
+                ptx::tmem_ld_wait();
+                reg_fence(v);
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    pk[e] = ptx::pack_bf16x2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+#pragma unroll
+                for (int v4 = 0; v4 < 4; ++v4)
+                    sts_u128(srow + (((h * 4 + v4) ^ (r & 7)) << 4),
+                             make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]));
+            }
+            ptx::tc_fence_before();
+            ptx::fence_proxy_async_smem();
+            ptx::named_bar(1, 256);
+            if (threadIdx.x == 0) {
+                ptx::tma_store_3d(&tm_dk, stage, 0, kv0, bh);
+                ptx::tma_store_3d(&tm_dv, stage + C::T_BYTES, 0, kv0, bh);
+                ptx::bulk_commit_group();
+            }
+            store_pending = true;
+        };
+        TileCursor c;
+        c.start(first, n_kvblocks, C::BN);
+        int prev_bh = 0, prev_kv0 = 0;
+        for (int t = 0; t < T; ++t) {
+            const int b = t & 1, s = t % C::QST;
+            const bool key_ok = c.kv0 + r < n;
+            // {-LSE2 pair, -D pair} per two of this warpgroup's queries
+            const uint32_t sst_a = ptx::smem_u32(sLD + s * 2 * C::BM + wg * 128);
+            const uint32_t rowp_a = ptx::smem_u32(sDS + b * C::DS_BYTES + wg * (C::BN * 128) + r * 128);
+            const uint32_t tS = tmem + lane_off + C::tm_s(b) + wg * 64;
+            const uint32_t tDP = tmem + lane_off + C::TM_DP + wg * 64;
+            wait_bounded(&bar_s_full[b], (t >> 1) & 1, g);
+            wait_bounded(&bar_ds_empty[b], ((t >> 1) & 1) ^ 1, g);
+            ptx::tc_fence_after();
+            // Phase 1, as soon as S^T is in: P^T = 2^(S^T c - LSE2), bf16 back into TMEM over S^T
+            // columns already read, fp32 kept for dS.
+            float pf[64];
+            {
+                uint32_t sv[2][16];
+                ptx::tmem_ld16(tS, sv[0]);
+                ptx::tmem_ld_wait();
+                reg_fence(sv[0]);
+#pragma unroll
+                for (int qt = 0; qt < 4; ++qt) {
+                    const int cur = qt & 1;
+                    if (qt < 3) ptx::tmem_ld16(tS + (qt + 1) * 16, sv[cur ^ 1]);
+                    uint2 nl[8];   // -LSE2 of queries (c, c + 1), c = 0, 2, ..., 14
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) nl[e] = lds_u64(sst_a + (qt * 16 + 2 * e) * 8);
+                    uint32_t pp[8];
+#pragma unroll
+                    for (int cc = 0; cc < 16; cc += 2) {
+                        const uint64_t x = ptx::fma_f32x2(
+                            ptx::f2_pack(__uint_as_float(sv[cur][cc]), __uint_as_float(sv[cur][cc + 1])), c2,
+                            ((uint64_t)nl[cc / 2].y << 32) | nl[cc / 2].x);
+                        float x0, x1;
+                        ptx::f2_unpack(x, x0, x1);
+                        float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+                        if (!key_ok) p0 = p1 = 0.f;
+                        pf[qt * 16 + cc] = p0;
+                        pf[qt * 16 + cc + 1] = p1;
+                        pp[cc / 2] = ptx::pack_bf16x2(p0, p1);
+                    }
+                    ptx::tmem_st8(tS + qt * 8, pp);
+                    if (qt < 3) {
+                        ptx::tmem_ld_wait();
+                        reg_fence(sv[cur ^ 1]);
+                    }
+                }
+            }
+            // The previous item's dK / dV, while this tile's dP^T and the previous tile's
+            // products run; before this tile's dS^T, which lets its dV / dK restart the
+            // accumulators.  Staged in the other dS^T buffer: the previous tile's dK and dQ^T,
+            // complete once dK / dV are, have read it, and the next tile's dS^T waits for the
+            // stores below.
+            if (c.it == 0 && c.li > 0) {
+                epilogue(c.li - 1, prev_bh, prev_kv0, sDS + (b ^ 1) * C::DS_BYTES);
+            } else if (store_pending) {   // the stores issued one tile ago read this dS^T buffer
+                if (threadIdx.x == 0) ptx::bulk_wait_group_read<0>();
+                ptx::named_bar(1, 256);
+                store_pending = false;
+            }
+            // Phase 2, once dP^T is in: dS^T = P^T o (dP^T - D), bf16 into shared memory.
+            wait_bounded(&bar_dp_full, t & 1, g);
+            ptx::tc_fence_after();
+            {
+                uint32_t dpv[2][16];
+                ptx::tmem_ld16(tDP, dpv[0]);
+                ptx::tmem_ld_wait();
+                reg_fence(dpv[0]);
+#pragma unroll
+                for (int qt = 0; qt < 4; ++qt) {
+                    const int cur = qt & 1;
+                    if (qt < 3) ptx::tmem_ld16(tDP + (qt + 1) * 16, dpv[cur ^ 1]);
+                    uint2 nd[8];   // -D of queries (c, c + 1)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) nd[e] = lds_u64(sst_a + (qt * 16 + 2 * e) * 8 + 8);
+                    uint32_t dsp[8];
+#pragma unroll
+                    for (int cc = 0; cc < 16; cc += 2) {
+                        const uint64_t dsq = ptx::mul_f32x2(
+                            ptx::f2_pack(pf[qt * 16 + cc], pf[qt * 16 + cc + 1]),
+                            ptx::add_f32x2(ptx::f2_pack(__uint_as_float(dpv[cur][cc]), __uint_as_float(dpv[cur][cc + 1])),
+                                           ((uint64_t)nd[cc / 2].y << 32) | nd[cc / 2].x));
+                        float ds0, ds1;
+                        ptx::f2_unpack(dsq, ds0, ds1);
+                        dsp[cc / 2] = ptx::pack_bf16x2(ds0, ds1);
+                    }
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        sts_u128(rowp_a + (((qt * 2 + h) ^ (r & 7)) << 4),
+                                 make_uint4(dsp[4 * h], dsp[4 * h + 1], dsp[4 * h + 2], dsp[4 * h + 3]));
+                    if (qt < 3) {
+                        ptx::tmem_ld_wait();
+                        reg_fence(dpv[cur ^ 1]);
+                    }
+                }
+            }
+            ptx::tmem_st_wait();
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&bar_ds_full);
+            prev_bh = c.bh;
+            prev_kv0 = c.kv0;
+            c.next(nq, first, stride, n_kvblocks, C::BN);
+        }
+        if (n_mine > 0) {
+            epilogue(n_mine - 1, prev_bh, prev_kv0, sDS);   // every product is done: any buffer
+            if (threadIdx.x == 0) ptx::bulk_wait_group<0>();   // complete before the CTA exits
+        }
+    } else if (WITH_DQ && warp < 10) {
+        // ---------------------------------------------------------------- dQ warps
+        const int r = (warp - 8) * 32 + lane;   // d column = TMEM lane of dQ^T
+        const uint32_t lane_off = (uint32_t)((warp - 8) * 32) << 16;
+        const bool leader = threadIdx.x == 256;
+        int chunk = 0;   // staging buffer = chunk & 1
+        TileCursor c;
+        c.start(first, n_kvblocks, C::BN);
+        for (int t = 0; t < T; ++t) {
+            const int b = t & 1;
+            wait_bounded(&bar_dq_full[b], (t >> 1) & 1, g);
+            ptx::tc_fence_after();
+            uint32_t v[4][32];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) ptx::tmem_ld32(tmem + lane_off + C::tm_s(b) + q * 32, v[q]);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int q = 0; q < 4; ++q) reg_fence(v[q]);
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&bar_dq_empty[b]);
+            // chunks of DQC_ROWS query rows, alternating between two staging buffers so that
+            // filling one overlaps the bulk reduce-add still reading the other
+#pragma unroll
+            for (int q = 0; q < C::BM / C::DQC_ROWS; ++q, ++chunk) {
+                // Chunks past N (only in an item's last tile) are skipped by every dQ thread
+                // alike: each staged chunk is one bulk group, which the buffer reuse counts on.
+                const int q0 = c.it * C::BM + q * C::DQC_ROWS;
+                if (q0 >= n) break;
+                const int rows = (n - q0) < C::DQC_ROWS ? (n - q0) : C::DQC_ROWS;
+                float *stage = sDQ + (chunk & 1) * (C::DQC_BYTES / 4);
+                if (leader) ptx::bulk_wait_group_read<1>();   // this buffer's last reduce has read it
+                ptx::named_bar(2, 64);
+                const uint32_t base = opaque(ptx::smem_u32(stage) + r * 4);
+#pragma unroll
+                for (int qq = 0; qq < C::DQC_ROWS; ++qq)
+                    sts_f32(base + qq * D * 4, __uint_as_float(v[q * C::DQC_ROWS / 32][(q * C::DQC_ROWS) % 32 + qq]));
+                ptx::fence_proxy_async_smem();
+                ptx::named_bar(2, 64);
+                if (leader) {
+                    ptx::bulk_reduce_add_f32(dq_acc + ((size_t)c.bh * n + q0) * D, stage, (uint32_t)rows * D * 4);
+                    ptx::bulk_commit_group();
+                }
+            }
+            c.next(nq, first, stride, n_kvblocks, C::BN);
+        }
+        if (leader) ptx::bulk_wait_group<0>();
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == C::MMA_WARP) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 512);
+    }
+}
+
 // ------------------------------------------------------------------ 2''. dK / dV only, d = 128
 // The deterministic mode's dK, dV pass for d = 128 with 128-query tiles, so that its four
 // products run at N = 128 (S^T and dP^T at N = 64 take as long as at N = 128).  TMEM holds dK,
@@ -1561,6 +2070,45 @@ cudaError_t launch_main_wide(const BwdArgs &a, cudaStream_t stream)
     return cudaGetLastError();
 }
 
+int bwd_sm_count()
+{
+    static int cached[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return 148;
+    if (cached[dev] == 0) {
+        int sms = 0;
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cached[dev] = sms > 0 ? sms : 148;
+    }
+    return cached[dev];
+}
+
+template <bool WITH_DQ>
+cudaError_t launch_main_persist(const BwdArgs &a, cudaStream_t stream)
+{
+    using C = PersistBwdCfg;
+    cudaError_t e = cudaFuncSetAttribute(bwd_main_persist_kernel<WITH_DQ>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int n_kvblocks = (a.n + C::BN - 1) / C::BN;
+    const long long items = (long long)n_kvblocks * a.bh;
+    const long long ctas = std::min<long long>(items, bwd_sm_count());
+    bwd_main_persist_kernel<WITH_DQ><<<(unsigned)ctas, C::THREADS, C::SMEM_BYTES, stream>>>(
+        a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dk, a.tm_dv, a.stats, a.dq_acc, a.n, a.n_pad, n_kvblocks,
+        (int)items, a.scale, a.status);
+    return cudaGetLastError();
+}
+
+// d = 64 main kernel: the persistent variant where each key block has only a few query tiles.
+template <bool WITH_DQ>
+cudaError_t launch_main_d64(const BwdArgs &a, cudaStream_t stream)
+{
+    const int nq = (a.n + 127) / 128;
+    if (nq >= 2 && a.n <= kBwdPersistentMaxN) return launch_main_persist<WITH_DQ>(a, stream);
+    return launch_main_wide<WITH_DQ>(a, stream);
+}
+
 cudaError_t launch_dkdv_d128(const BwdArgs &a, cudaStream_t stream)
 {
     using C = D128Cfg;
@@ -1577,7 +2125,7 @@ cudaError_t launch_dkdv_d128(const BwdArgs &a, cudaStream_t stream)
 
 cudaError_t launch_bwd_main(const BwdArgs &a, cudaStream_t stream)
 {
-    return a.d == 64 ? launch_main_wide<true>(a, stream) : launch_main_d<128, true>(a, stream);
+    return a.d == 64 ? launch_main_d64<true>(a, stream) : launch_main_d<128, true>(a, stream);
 }
 
 template <int D>
@@ -1600,7 +2148,7 @@ cudaError_t launch_bwd_deterministic(const BwdArgs &a, cudaStream_t stream)
     cudaError_t e = a.d == 64 ? launch_preprocess_d<64>(a, false, stream)
                               : launch_preprocess_d<128>(a, false, stream);
     if (e == cudaSuccess)
-        e = a.d == 64 ? launch_main_wide<false>(a, stream) : launch_dkdv_d128(a, stream);
+        e = a.d == 64 ? launch_main_d64<false>(a, stream) : launch_dkdv_d128(a, stream);
     if (e == cudaSuccess) e = a.d == 64 ? launch_dq_d<64>(a, stream) : launch_dq_d<128>(a, stream);
     return e;
 }

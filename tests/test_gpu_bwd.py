@@ -67,6 +67,18 @@ def test_bwd_edge_sizes(n, d):
         check_grad(name, got[name], ref[name], f"N={n} d={d}")
 
 
+@pytest.mark.parametrize("n", [4097, 4200])
+def test_bwd_d64_long_sequence(n):
+    """d_k = 64 past 4096 keys runs the one-CTA-per-key-block kernel instead of the persistent
+    one that the shorter sizes above use; ragged last tiles in both directions."""
+    inp = make_qkv(1, 2, n, 64, seed=9500 + n)
+    scale = 0.125
+    got = run_fwd_bwd(inp, scale)
+    ref = oracle.bwd(inp["q"], inp["k"], inp["v"], inp["do"], scale)
+    for name in ("dq", "dk", "dv"):
+        check_grad(name, got[name], ref[name], f"N={n} d=64")
+
+
 @pytest.mark.parametrize("d", [64, 128])
 def test_bwd_wide_logits_and_scale(d):
     inp = make_qkv(2, 2, 700, d, seed=21, qk_std=2.0)
