@@ -514,7 +514,14 @@ def run_ours(args, world, rank, local):
     achieved = main_flops / (local_res["bwd_main_ms"] * 1e-3) / 1e12
     peak = peaks["bf16_tflops_sustained"]
     units = B * H * math.ceil(N / 128) * math.ceil(N / 64)   # (key tile, query tile) pairs
-    traffic = profiled_traffic(units)
+    # the committed counters are those of the d_k = 128 main kernel; other kernels report none
+    traffic = profiled_traffic(units) if D == 128 else None
+    if D == 128:
+        main_kernel = "bwd_main_kernel<128>"
+    elif 128 < N <= 4096:
+        main_kernel = "bwd_main_persist_kernel"
+    else:
+        main_kernel = "bwd_main_wide_kernel"
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -534,7 +541,7 @@ def run_ours(args, world, rank, local):
         "fwd_pct_of_bf16_peak": 100.0 * per_gpu_fwd / peaks["bf16_tflops"],
         "bwd_pct_of_bf16_peak": 100.0 * per_gpu_bwd / peaks["bf16_tflops"],
         "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback",
-        "roofline": {"kernel": "bwd_main_kernel<128>" if D == 128 else "bwd_main_wide_kernel",
+        "roofline": {"kernel": main_kernel,
                      "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "note": f"peak = {peak_src} sustained dense bf16; achieved = 10*B*H*N^2*d "
