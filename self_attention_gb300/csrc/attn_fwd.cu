@@ -11,8 +11,9 @@
 // as LSE = log sum_j exp(scale * q_i . k_j).
 //
 // Blackwell mapping of fwd_kernel<D, NQ> (one CTA = NQ query tiles of 128 rows of one head;
-// NQ = 2 for d = 128, shown here; NQ = 1 for d = 64, where the softmax ALU work per tile equals
-// the matrix work and two one-tile CTAs per SM overlap better than two tiles in one CTA):
+// used for d = 128 with NQ = 2, shown here.  d = 64, where the softmax work per tile equals the
+// matrix work, runs one tile per CTA and two CTAs per SM: fwd_sp_kernel, and for short
+// sequences with many tiles fwd_persistent_kernel, below):
 //   warp 8      TMA producer: Q tiles once, then a ring of K and V tiles (128 keys each).
 //   warp 9      tcgen05 issuer: S_t = Q_t K_j^T into TMEM (fp32), then O_t += P_t V_j with
 //               P_t read from TMEM (bf16, written over S_t) and V_j from shared memory.
@@ -37,8 +38,9 @@ constexpr float kLn2 = 0.6931471805599453f;
 // many powers of two; in between, probabilities may reach 2^kTau, far from fp32/bf16 limits.
 constexpr float kTau = 8.0f;
 // d = 64 runs one 128-row query tile per CTA, two CTAs per SM; up to this sequence length
-// the CTAs are persistent (the per-item latencies dominate there), beyond it one CTA per tile.
-constexpr int kFwdPersistentMaxN = 2048;
+// (and with more tiles than resident CTAs) the CTAs are persistent (the per-item latencies
+// dominate there), beyond it one CTA per tile (fwd_sp_kernel).
+constexpr int kFwdPersistentMaxN = 768;
 
 template <int D, int NQ_>
 struct FwdCfg {
@@ -322,6 +324,287 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::THREADS, FwdCfg<D, NQ>::MIN_BLO
                 for (int v4 = 0; v4 < 4; ++v4)
                     dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
             }
+        }
+        if (row < n) lse[(size_t)bh * n + row] = (m + log2f(l)) * kLn2;
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == C::MMA_WARP) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, C::TM_COLS);
+    }
+}
+
+// fwd_sp_kernel: d = 64, one 128-row query tile per CTA, two CTAs per SM, with P in TMEM
+// columns of its own instead of over S.  S of key tile j + 1 is then issued as soon as the
+// softmax warps have read S_j out of TMEM, and runs under their exponentials; only P_j (and a
+// rescale of O) waits for the P V product of tile j - 1.
+//   warp 4      TMA producer: Q once, then a ring of K and V tiles.
+//   warp 5      tcgen05 issuer: S_{j+1} = Q K_{j+1}^T once S_j has been read, O += P_j V_j once
+//               P_j is in.
+//   warps 0-3   softmax, thread = query row: read S_j, running max and sum as fwd_kernel, P_j
+//               (bf16) into the P columns once P V of tile j - 1 is done with them; at the end
+//               O / l through the idle Q tile to global memory by one TMA tensor store.
+// TMEM columns: S [0,128), O [128,192), P [192,256).
+struct FwdSpCfg {
+    static constexpr int D = 64;
+    static constexpr int BM = 128, BN = 128;
+    static constexpr int STAGES = 2;
+    static constexpr int Q_BYTES = BM * D * 2;
+    static constexpr int KV_BYTES = BN * D * 2;
+    static constexpr int SMEM_BYTES = Q_BYTES + 2 * STAGES * KV_BYTES + 1024;
+    static constexpr int THREADS = 192;
+    static constexpr int TMA_WARP = 4, MMA_WARP = 5;
+    static constexpr uint32_t TM_O = 128, TM_P = 192, TM_COLS = 256;
+};
+
+__global__ void __launch_bounds__(192, 2)
+    fwd_sp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                  float *__restrict__ lse, int n, int n_qblocks, float scale_log2, int *status)
+{
+    using C = FwdSpCfg;
+    constexpr int D = C::D;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    uint8_t *sQ = smem;
+    uint8_t *sK = sQ + C::Q_BYTES;
+    uint8_t *sV = sK + C::STAGES * C::KV_BYTES;
+
+    __shared__ uint64_t bar_q;
+    __shared__ uint64_t bar_kf[C::STAGES], bar_ke[C::STAGES], bar_vf[C::STAGES], bar_ve[C::STAGES];
+    __shared__ uint64_t bar_s, bar_sread, bar_p, bar_pv, bar_done;
+    __shared__ uint32_t tmem_sh;
+    __shared__ int abort_sh;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.x / n_qblocks;
+    const int q0 = (blockIdx.x % n_qblocks) * C::BM;
+    const int nkv = (n + C::BN - 1) / C::BN;
+    const Guard g{&abort_sh, status, kWaitLimitNs};
+
+    if (threadIdx.x == 0) {
+        abort_sh = 0;
+        ptx::mbar_init(&bar_q, 1);
+        for (int s = 0; s < C::STAGES; ++s) {
+            ptx::mbar_init(&bar_kf[s], 1);
+            ptx::mbar_init(&bar_ke[s], 1);
+            ptx::mbar_init(&bar_vf[s], 1);
+            ptx::mbar_init(&bar_ve[s], 1);
+        }
+        ptx::mbar_init(&bar_s, 1);
+        ptx::mbar_init(&bar_sread, 128);
+        ptx::mbar_init(&bar_p, 128);
+        ptx::mbar_init(&bar_pv, 1);
+        ptx::mbar_init(&bar_done, 1);
+        ptx::fence_mbar_init();
+    }
+    if (warp == C::MMA_WARP) {
+        ptx::tmem_alloc(&tmem_sh, C::TM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = tmem_sh;
+
+    if (warp == C::TMA_WARP) {
+        // ---------------------------------------------------------------- TMA producer
+        if (ptx::elect_one()) {
+            ptx::tma_prefetch_desc(&tm_q);
+            ptx::tma_prefetch_desc(&tm_k);
+            ptx::tma_prefetch_desc(&tm_v);
+            ptx::mbar_arrive_expect_tx(&bar_q, C::Q_BYTES);
+            ptx::tma_load_3d(sQ, &tm_q, &bar_q, 0, q0, bh);
+            for (int j = 0; j < nkv; ++j) {
+                const int s = j % C::STAGES;
+                const uint32_t ph = (j / C::STAGES) & 1;
+                wait_bounded(&bar_ke[s], ph ^ 1, g);
+                ptx::mbar_arrive_expect_tx(&bar_kf[s], C::KV_BYTES);
+                ptx::tma_load_3d(sK + s * C::KV_BYTES, &tm_k, &bar_kf[s], 0, j * C::BN, bh);
+                wait_bounded(&bar_ve[s], ph ^ 1, g);
+                ptx::mbar_arrive_expect_tx(&bar_vf[s], C::KV_BYTES);
+                ptx::tma_load_3d(sV + s * C::KV_BYTES, &tm_v, &bar_vf[s], 0, j * C::BN, bh);
+            }
+            // Do not leave the CTA with copies in flight (matters only after a timeout).
+            wait_bounded(&bar_q, 0, g);
+            for (int j = (nkv > C::STAGES ? nkv - C::STAGES : 0); j < nkv; ++j) {
+                const int s = j % C::STAGES;
+                const uint32_t ph = (j / C::STAGES) & 1;
+                wait_bounded(&bar_kf[s], ph, g);
+                wait_bounded(&bar_vf[s], ph, g);
+            }
+        }
+    } else if (warp == C::MMA_WARP) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (ptx::elect_one()) {
+            const uint32_t idS = ptx::idesc_bf16_f32(128, C::BN, false, false);
+            const uint32_t idO = ptx::idesc_bf16_f32(128, D, false, true);
+            const uint32_t q_base = ptx::smem_u32(sQ), k_base = ptx::smem_u32(sK),
+                           v_base = ptx::smem_u32(sV);
+            // S = Q K_j^T: both operands K-major (d contiguous).
+            auto issue_s = [&](int s) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    ptx::mma_ss(tmem, ptx::sdesc_sw128(q_base + kk * 32, 16, 1024),
+                                ptx::sdesc_sw128(k_base + s * C::KV_BYTES + kk * 32, 16, 1024), idS,
+                                kk > 0 ? 1u : 0u);
+            };
+            // O += P V_j: P from its TMEM columns (8 columns = 16 keys per step), V MN-major.
+            auto issue_pv = [&](int s, bool acc) {
+#pragma unroll
+                for (int kk = 0; kk < C::BN / 16; ++kk)
+                    ptx::mma_ts(tmem + C::TM_O, tmem + C::TM_P + kk * 8,
+                                ptx::sdesc_sw128(v_base + s * C::KV_BYTES + kk * 2048, C::BN * 128, 1024), idO,
+                                (acc || kk > 0) ? 1u : 0u);
+            };
+            wait_bounded(&bar_q, 0, g);
+            wait_bounded(&bar_kf[0], 0, g);
+            ptx::tc_fence_after();
+            issue_s(0);
+            ptx::mma_commit(&bar_s);
+            ptx::mma_commit(&bar_ke[0]);
+            for (int j = 0; j < nkv; ++j) {
+                const int s = j % C::STAGES;
+                if (j + 1 < nkv) {   // S_{j+1} over S_j once the softmax has read it
+                    const int sn = (j + 1) % C::STAGES;
+                    wait_bounded(&bar_sread, j & 1, g);
+                    wait_bounded(&bar_kf[sn], ((j + 1) / C::STAGES) & 1, g);
+                    ptx::tc_fence_after();
+                    issue_s(sn);
+                    ptx::mma_commit(&bar_s);
+                    ptx::mma_commit(&bar_ke[sn]);
+                }
+                wait_bounded(&bar_vf[s], (j / C::STAGES) & 1, g);
+                wait_bounded(&bar_p, j & 1, g);
+                ptx::tc_fence_after();
+                issue_pv(s, j > 0);
+                ptx::mma_commit(&bar_pv);   // P and O free again; after the last tile: O final
+                ptx::mma_commit(&bar_ve[s]);
+            }
+            // Every MMA must have finished before TMEM is released (matters after a timeout).
+            ptx::mma_commit(&bar_done);
+            wait_bounded(&bar_done, 0, g);
+        }
+    } else {
+        // ---------------------------------------------------------------- softmax warpgroup
+        const int r_local = warp * 32 + lane;   // row of the tile = TMEM lane
+        const int row = q0 + r_local;
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const uint32_t tS = tmem + lane_off, tO = tmem + lane_off + C::TM_O, tP = tmem + lane_off + C::TM_P;
+        float m = -INFINITY, l = 0.f;
+        for (int j = 0; j < nkv; ++j) {
+            wait_bounded(&bar_s, j & 1, g);
+            ptx::tc_fence_after();
+            uint32_t r[128];
+            ptx::tmem_ld32_at<0>(tS + 0, r);
+            ptx::tmem_ld32_at<32>(tS + 32, r);
+            ptx::tmem_ld32_at<64>(tS + 64, r);
+            ptx::tmem_ld32_at<96>(tS + 96, r);
+            ptx::tmem_ld_wait();
+            reg_fence(r);
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&bar_sread);   // S may take the next tile's product
+            // keys >= n (only in the last tile) take no weight
+            const int valid = n - j * C::BN;
+            if (valid < C::BN) {
+#pragma unroll
+                for (int i = 0; i < 128; ++i)
+                    if (i >= valid) r[i] = __float_as_uint(-INFINITY);
+            }
+            float mx[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) mx[u] = __uint_as_float(r[u]);
+#pragma unroll
+            for (int i = 8; i < 128; i += 2)
+                mx[(i >> 1) & 7] = ptx::max3(mx[(i >> 1) & 7], __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+            const float smax = ptx::max3(ptx::max3(mx[0], mx[1], mx[2]), ptx::max3(mx[3], mx[4], mx[5]),
+                                         fmaxf(mx[6], mx[7]));
+            const float mt = smax * scale_log2;
+            float m_new = m, alpha = 1.f;
+            bool rescale = false;
+            if (j == 0) {
+                m_new = mt;
+            } else if (__any_sync(0xffffffffu, mt > m + kTau)) {
+                m_new = fmaxf(m, mt);
+                alpha = ptx::ex2(m - m_new);
+                rescale = true;
+            }
+            const float neg_m = -m_new;
+            const uint64_t c2 = ptx::f2_pack(scale_log2, scale_log2), nm2 = ptx::f2_pack(neg_m, neg_m);
+            uint64_t acc2[2] = {ptx::f2_pack(0.f, 0.f), ptx::f2_pack(0.f, 0.f)};
+            // P = 2^(x - m) as bf16 pairs, packed into r[0, 64) (each pair lands at or below the
+            // slots it was computed from)
+#pragma unroll
+            for (int i = 0; i < 128; i += 2) {
+                const uint64_t t = ptx::fma_f32x2(ptx::f2_pack(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), c2, nm2);
+                float t0, t1;
+                ptx::f2_unpack(t, t0, t1);
+                const float p0 = ptx::ex2(t0), p1 = ptx::ex2(t1);
+                acc2[(i >> 1) & 1] = ptx::add_f32x2(acc2[(i >> 1) & 1], ptx::f2_pack(p0, p1));
+                r[i >> 1] = ptx::pack_bf16x2(p0, p1);
+            }
+            float sum[4];
+            ptx::f2_unpack(acc2[0], sum[0], sum[1]);
+            ptx::f2_unpack(acc2[1], sum[2], sum[3]);
+            l = l * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
+            m = m_new;
+            // P of tile j - 1 has been multiplied into O: its columns and O are ours again
+            if (j > 0) wait_bounded(&bar_pv, (j - 1) & 1, g);
+            ptx::tc_fence_after();
+            if (rescale) {
+#pragma unroll
+                for (int c = 0; c < D; c += 32) {
+                    uint32_t ov[32];
+                    ptx::tmem_ld32(tO + c, ov);
+                    ptx::tmem_ld_wait();
+                    reg_fence(ov);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                    ptx::tmem_st32(tO + c, ov);
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) pk[i] = r[h * 32 + i];
+                ptx::tmem_st32(tP + h * 32, pk);
+            }
+            ptx::tmem_st_wait();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&bar_p);
+        }
+
+        // epilogue: O = O_acc / l (bf16) into the idle Q tile (128-byte swizzle: 16-byte chunk c
+        // of row r at chunk c ^ (r % 8)), one TMA tensor store (rows past N clipped);
+        // LSE = (m + log2 l) ln 2
+        wait_bounded(&bar_pv, (nkv - 1) & 1, g);
+        ptx::tc_fence_after();
+        const float inv_l = 1.f / l;
+        const uint32_t srow = ptx::smem_u32(sQ) + r_local * 128;
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+            uint32_t ov[32];
+            ptx::tmem_ld32(tO + c, ov);
+            ptx::tmem_ld_wait();
+            reg_fence(ov);
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                pk[i] = ptx::pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+                sts_u128(srow + ((((c >> 3) + v4) ^ (r_local & 7)) << 4),
+                         make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]));
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::named_bar(1, 128);
+        if (threadIdx.x == 0) {
+            ptx::tma_store_3d(&tm_o, sQ, 0, q0, bh);
+            ptx::bulk_commit_group();
+            ptx::bulk_wait_group<0>();   // complete before the CTA exits
         }
         if (row < n) lse[(size_t)bh * n + row] = (m + log2f(l)) * kLn2;
     }
@@ -698,13 +981,27 @@ cudaError_t launch_fwd_d(const FwdArgs &a, cudaStream_t stream)
     return cudaGetLastError();
 }
 
+cudaError_t launch_fwd_sp(const FwdArgs &a, cudaStream_t stream)
+{
+    using C = FwdSpCfg;
+    cudaError_t e = cudaFuncSetAttribute(fwd_sp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int n_qblocks = (a.n + C::BM - 1) / C::BM;
+    const long long ctas = (long long)n_qblocks * a.bh;
+    fwd_sp_kernel<<<(unsigned)ctas, C::THREADS, C::SMEM_BYTES, stream>>>(
+        a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.lse, a.n, n_qblocks, a.scale * kLog2e, a.status);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_fwd(const FwdArgs &a, cudaStream_t stream)
 {
     if (a.d == 128) return launch_fwd_d<128, 2>(a, stream);
-    if (a.n <= kFwdPersistentMaxN) return launch_fwd_persistent<64>(a, stream);
-    return launch_fwd_d<64, 1>(a, stream);
+    const long long tiles = (long long)a.bh * ((a.n + 127) / 128);
+    if (a.n <= kFwdPersistentMaxN && tiles > 2LL * sm_count()) return launch_fwd_persistent<64>(a, stream);
+    return launch_fwd_sp(a, stream);
 }
 
 }  // namespace attn

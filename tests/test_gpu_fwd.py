@@ -67,6 +67,20 @@ def test_fwd_edge_sizes(n, d):
     check_lse(lse, lse_ref, f"N={n} d={d}")
 
 
+@pytest.mark.parametrize("n", [129, 300, 700])
+def test_fwd_d64_many_short_tiles(n):
+    """d_k = 64 with more query tiles than resident CTAs and a short sequence: the persistent
+    forward, whose CTAs walk several (head, query block) items; ragged last blocks."""
+    inp = make_qkv(2, 96, n, 64, seed=7500 + n, with_do=False)
+    o, lse = run_fwd(inp, 0.125)
+    sel = np.arange(0, 192, 7)   # every 7th head of the 192, in full
+    pick = lambda t: t.reshape(192, n, 64)[sel].reshape(1, -1, n, 64)
+    ref_in = {x: pick(inp[x]) for x in ("q", "k", "v")}
+    o_ref, lse_ref, a_abs = oracle_fwd(ref_in, 0.125)
+    check_o(o.reshape(192, n, 64)[sel][None], o_ref, a_abs, f"N={n} d=64 many tiles")
+    check_lse(lse.reshape(192, n)[sel][None], lse_ref, f"N={n} d=64 many tiles")
+
+
 @pytest.mark.parametrize("d", [64, 128])
 def test_fwd_wide_logits(d):
     """Q, K ~ N(0, 2^2) as in the long-text workload: logits with standard deviation 4 move
