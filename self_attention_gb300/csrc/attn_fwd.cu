@@ -12,8 +12,8 @@
 //
 // Blackwell mapping of fwd_kernel<D, NQ> (one CTA = NQ query tiles of 128 rows of one head;
 // used for d = 128 with NQ = 2, shown here.  d = 64, where the softmax work per tile equals the
-// matrix work, runs one tile per CTA and two CTAs per SM: fwd_sp_kernel, and for short
-// sequences with many tiles fwd_persistent_kernel, below):
+// matrix work, runs one tile per CTA and two CTAs per SM: fwd_persistent_kernel, or
+// fwd_sp_kernel where there are fewer tiles than resident CTAs, below):
 //   warp 8      TMA producer: Q tiles once, then a ring of K and V tiles (128 keys each).
 //   warp 9      tcgen05 issuer: S_t = Q_t K_j^T into TMEM (fp32), then O_t += P_t V_j with
 //               P_t read from TMEM (bf16, written over S_t) and V_j from shared memory.
@@ -37,10 +37,6 @@ constexpr float kLn2 = 0.6931471805599453f;
 // The running maximum is only moved (and O rescaled) when a tile raises it by more than this
 // many powers of two; in between, probabilities may reach 2^kTau, far from fp32/bf16 limits.
 constexpr float kTau = 8.0f;
-// d = 64 runs one 128-row query tile per CTA, two CTAs per SM; up to this sequence length
-// (and with more tiles than resident CTAs) the CTAs are persistent (the per-item latencies
-// dominate there), beyond it one CTA per tile (fwd_sp_kernel).
-constexpr int kFwdPersistentMaxN = 768;
 
 template <int D, int NQ_>
 struct FwdCfg {
@@ -622,16 +618,16 @@ __global__ void __launch_bounds__(192, 2)
 // next item, the tail of the previous one and the other CTA's work hide each other's latency.
 //   warp 4      TMA: Q of each item into one of two Q buffers, K/V tiles through one ring that
 //               runs across items.
-//   warp 5      tcgen05: S = Q K_j^T, O_b += P V_j (b = item parity: two O accumulators, so
-//               an item's products start while the previous item's O is still being written
-//               out); the next S, of this item or the next, follows each P V at once.
-//   warps 0-3   softmax as above, then the epilogue of the item from O_b: the normalised bf16
-//               tile goes into the item's Q buffer (free once the item's last S has read it),
-//               in the 128-byte-swizzled layout, and leaves with one TMA tensor store (rows
-//               past N are clipped); the Q buffer returns to the producer once the store has
-//               read it.  (One thread per 128-byte row, storing straight to global, makes every
-//               warp store touch 32 lines.)
-// TMEM columns: S [0,128), O_0 [128,128+d), O_1 [128+d,128+2d).
+//   warp 5      tcgen05: S = Q K_j^T, then O += P V_j; as in fwd_sp_kernel the next S, of this
+//               item or the next, is issued as soon as the softmax warps have read S, and runs
+//               under their exponentials.
+//   warps 0-3   softmax as fwd_sp_kernel (P in TMEM columns of its own), then the epilogue of
+//               the item: the normalised bf16 tile goes into the item's Q buffer (free once the
+//               item's last S has read it), in the 128-byte-swizzled layout, and leaves with
+//               one TMA tensor store (rows past N are clipped); the Q buffer returns to the
+//               producer once the store has read it.  The next item's first P V (accumulate
+//               off) follows the softmax warps' next P, after this epilogue has read O.
+// TMEM columns: S [0,128), O [128,128+d), P [128+d,128+d+64).
 template <int D>
 struct PersistCfg {
     static constexpr int BM = 128, BN = 128;
@@ -641,8 +637,8 @@ struct PersistCfg {
     static constexpr int SMEM_BYTES = 2 * Q_BYTES + 2 * STAGES * KV_BYTES + 1024;
     static constexpr int THREADS = 192;
     static constexpr int TMA_WARP = 4, MMA_WARP = 5;
-    static constexpr uint32_t TM_O = 128;
-    static constexpr uint32_t TM_COLS = 128 + 2 * D <= 256 ? 256 : 512;
+    static constexpr uint32_t TM_O = 128, TM_P = 128 + D;
+    static constexpr uint32_t TM_COLS = 128 + D + 64 <= 256 ? 256 : 512;
 };
 
 template <int D>
@@ -661,7 +657,7 @@ __global__ void __launch_bounds__(192, 2)
 
     __shared__ uint64_t bar_qf[2], bar_qfree[2];
     __shared__ uint64_t bar_kf[C::STAGES], bar_ke[C::STAGES], bar_vf[C::STAGES], bar_ve[C::STAGES];
-    __shared__ uint64_t bar_s, bar_p, bar_of[2], bar_oe[2], bar_done;
+    __shared__ uint64_t bar_s, bar_sread, bar_p, bar_pv, bar_done;
     __shared__ uint32_t tmem_sh;
     __shared__ int abort_sh;
 
@@ -675,8 +671,6 @@ __global__ void __launch_bounds__(192, 2)
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(&bar_qf[b], 1);
             ptx::mbar_init(&bar_qfree[b], 1);
-            ptx::mbar_init(&bar_of[b], 1);
-            ptx::mbar_init(&bar_oe[b], 128);
         }
         for (int s = 0; s < C::STAGES; ++s) {
             ptx::mbar_init(&bar_kf[s], 1);
@@ -685,7 +679,9 @@ __global__ void __launch_bounds__(192, 2)
             ptx::mbar_init(&bar_ve[s], 1);
         }
         ptx::mbar_init(&bar_s, 1);
+        ptx::mbar_init(&bar_sread, 128);
         ptx::mbar_init(&bar_p, 128);
+        ptx::mbar_init(&bar_pv, 1);
         ptx::mbar_init(&bar_done, 1);
         ptx::fence_mbar_init();
     }
@@ -752,13 +748,12 @@ __global__ void __launch_bounds__(192, 2)
                     ptx::mma_ss(tmem, a, b, idS, kk > 0 ? 1u : 0u);
                 }
             };
-            auto issue_pv = [&](int ob, int s, bool acc) {
+            auto issue_pv = [&](int s, bool acc) {
 #pragma unroll
                 for (int kk = 0; kk < C::BN / 16; ++kk) {
                     const uint64_t b =
                         ptx::sdesc_sw128(v_base + s * C::KV_BYTES + kk * 2048, C::BN * 128, 1024);
-                    ptx::mma_ts(tmem + C::TM_O + ob * D, tmem + kk * 8, b, idO,
-                                (acc || kk > 0) ? 1u : 0u);
+                    ptx::mma_ts(tmem + C::TM_O, tmem + C::TM_P + kk * 8, b, idO, (acc || kk > 0) ? 1u : 0u);
                 }
             };
             // S of global step kt (item li, key tile j)
@@ -774,20 +769,22 @@ __global__ void __launch_bounds__(192, 2)
             if (first < n_items) next_s(0, 0, 0);
             int kt = 0, li = 0;
             for (int item = first; item < n_items; item += stride, ++li) {
-                const int ob = li & 1;
                 for (int j = 0; j < nkv; ++j, ++kt) {
                     const int s = kt % C::STAGES;
+                    // the next S, of this item or the next, over S once the softmax has read it
+                    if (j + 1 < nkv || item + stride < n_items) {
+                        wait_bounded(&bar_sread, kt & 1, g);
+                        if (j + 1 < nkv)
+                            next_s(li, j + 1, kt + 1);
+                        else
+                            next_s(li + 1, 0, kt + 1);
+                    }
                     wait_bounded(&bar_vf[s], (kt / C::STAGES) & 1, g);
-                    if (j == 0) wait_bounded(&bar_oe[ob], ((li >> 1) & 1) ^ 1, g);  // O_b written out
                     wait_bounded(&bar_p, kt & 1, g);
                     ptx::tc_fence_after();
-                    issue_pv(ob, s, j > 0);
+                    issue_pv(s, j > 0);
+                    ptx::mma_commit(&bar_pv);   // P and O free again; after an item's last tile: O final
                     ptx::mma_commit(&bar_ve[s]);
-                    if (j == nkv - 1) ptx::mma_commit(&bar_of[ob]);
-                    if (j + 1 < nkv)
-                        next_s(li, j + 1, kt + 1);
-                    else if (item + stride < n_items)
-                        next_s(li + 1, 0, kt + 1);
                 }
             }
             // Every MMA must have finished before TMEM is released (matters after a timeout).
@@ -797,14 +794,13 @@ __global__ void __launch_bounds__(192, 2)
     } else {
         // ---------------------------------------------------------------- softmax warpgroup
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-        const uint32_t tS = tmem + lane_off;
+        const uint32_t tS = tmem + lane_off, tO = tmem + lane_off + C::TM_O, tP = tmem + lane_off + C::TM_P;
         const int r_local = warp * 32 + lane;   // row of the tile = TMEM lane
         int kt = 0, li = 0;
         for (int item = first; item < n_items; item += stride, ++li) {
             const int bh = item / n_qblocks, q0 = (item % n_qblocks) * C::BM;
             const int row = q0 + r_local;
-            const int ob = li & 1, qb = li & 1;
-            const uint32_t tO = tmem + lane_off + C::TM_O + ob * D;
+            const int qb = li & 1;
             float m = -INFINITY, l = 0.f;
             for (int j = 0; j < nkv; ++j, ++kt) {
                 wait_bounded(&bar_s, kt & 1, g);
@@ -816,6 +812,8 @@ __global__ void __launch_bounds__(192, 2)
                 ptx::tmem_ld32_at<96>(tS + 96, r);
                 ptx::tmem_ld_wait();
                 reg_fence(r);
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(&bar_sread);   // S may take the next product
                 const int valid = n - j * C::BN;
                 if (valid < C::BN) {
 #pragma unroll
@@ -843,29 +841,25 @@ __global__ void __launch_bounds__(192, 2)
                 const float neg_m = -m_new;
                 const uint64_t c2 = ptx::f2_pack(scale_log2, scale_log2), nm2 = ptx::f2_pack(neg_m, neg_m);
                 uint64_t acc2[2] = {ptx::f2_pack(0.f, 0.f), ptx::f2_pack(0.f, 0.f)};
+                // P = 2^(x - m) as bf16 pairs, packed into r[0, 64)
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        const uint64_t t = ptx::fma_f32x2(
-                            ptx::f2_pack(__uint_as_float(r[ch * 32 + i]), __uint_as_float(r[ch * 32 + i + 1])), c2, nm2);
-                        float t0, t1;
-                        ptx::f2_unpack(t, t0, t1);
-                        const float p0 = ptx::ex2(t0), p1 = ptx::ex2(t1);
-                        acc2[(i >> 1) & 1] = ptx::add_f32x2(acc2[(i >> 1) & 1], ptx::f2_pack(p0, p1));
-                        pk[i >> 1] = ptx::pack_bf16x2(p0, p1);
-                    }
-                    ptx::tmem_st16(tS + ch * 16, pk);
+                for (int i = 0; i < 128; i += 2) {
+                    const uint64_t t = ptx::fma_f32x2(ptx::f2_pack(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), c2, nm2);
+                    float t0, t1;
+                    ptx::f2_unpack(t, t0, t1);
+                    const float p0 = ptx::ex2(t0), p1 = ptx::ex2(t1);
+                    acc2[(i >> 1) & 1] = ptx::add_f32x2(acc2[(i >> 1) & 1], ptx::f2_pack(p0, p1));
+                    r[i >> 1] = ptx::pack_bf16x2(p0, p1);
                 }
                 float sum[4];
                 ptx::f2_unpack(acc2[0], sum[0], sum[1]);
                 ptx::f2_unpack(acc2[1], sum[2], sum[3]);
                 l = l * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
                 m = m_new;
+                // the previous P V is done with the P columns and O
+                if (kt > 0) wait_bounded(&bar_pv, (kt - 1) & 1, g);
+                ptx::tc_fence_after();
                 if (rescale) {
-                    // O_b holds this item's partial sums up to key tile j - 1 (its P V for
-                    // tile j is issued only after this arrival).
 #pragma unroll
                     for (int c = 0; c < D; c += 32) {
                         uint32_t ov[32];
@@ -877,15 +871,22 @@ __global__ void __launch_bounds__(192, 2)
                         ptx::tmem_st32(tO + c, ov);
                     }
                 }
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) pk[i] = r[h * 32 + i];
+                    ptx::tmem_st32(tP + h * 32, pk);
+                }
                 ptx::tmem_st_wait();
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(&bar_p);
             }
 
-            // epilogue of this item: O = O_b / l (bf16) into the Q buffer (128-byte swizzle:
-            // 16-byte chunk c of row r at chunk c ^ (r % 8)), then one TMA store of the tile;
-            // LSE = (m + log2 l) ln 2
-            wait_bounded(&bar_of[ob], (li >> 1) & 1, g);
+            // epilogue of this item, once its last P V is done: O / l (bf16) into the Q buffer
+            // (128-byte swizzle: 16-byte chunk c of row r at chunk c ^ (r % 8)), then one TMA
+            // store of the tile; LSE = (m + log2 l) ln 2
+            wait_bounded(&bar_pv, (kt - 1) & 1, g);
             ptx::tc_fence_after();
             const float inv_l = 1.f / l;
             const uint32_t srow = ptx::smem_u32(sQ + qb * C::Q_BYTES) + r_local * 128;
@@ -908,8 +909,7 @@ __global__ void __launch_bounds__(192, 2)
                              make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]));
                 }
             }
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(&bar_oe[ob]);
+            ptx::tc_fence_before();   // O read: the next item's first P V may overwrite it
             ptx::fence_proxy_async_smem();
             ptx::named_bar(1, 128);
             if (threadIdx.x == 0) {
@@ -999,8 +999,11 @@ cudaError_t launch_fwd_sp(const FwdArgs &a, cudaStream_t stream)
 cudaError_t launch_fwd(const FwdArgs &a, cudaStream_t stream)
 {
     if (a.d == 128) return launch_fwd_d<128, 2>(a, stream);
+    // d = 64: one 128-row query tile per CTA, two CTAs per SM; persistent CTAs wherever there
+    // are more tiles than resident CTAs (equal to one CTA per tile at long sequences, ahead
+    // where items are short), else one CTA per tile
     const long long tiles = (long long)a.bh * ((a.n + 127) / 128);
-    if (a.n <= kFwdPersistentMaxN && tiles > 2LL * sm_count()) return launch_fwd_persistent<64>(a, stream);
+    if (tiles > 2LL * sm_count()) return launch_fwd_persistent<64>(a, stream);
     return launch_fwd_sp(a, stream);
 }
 

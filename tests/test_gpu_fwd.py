@@ -67,10 +67,10 @@ def test_fwd_edge_sizes(n, d):
     check_lse(lse, lse_ref, f"N={n} d={d}")
 
 
-@pytest.mark.parametrize("n", [129, 300, 700])
-def test_fwd_d64_many_short_tiles(n):
-    """d_k = 64 with more query tiles than resident CTAs and a short sequence: the persistent
-    forward, whose CTAs walk several (head, query block) items; ragged last blocks."""
+@pytest.mark.parametrize("n", [129, 300, 700, 2100])
+def test_fwd_d64_many_tiles(n):
+    """d_k = 64 with more query tiles than resident CTAs: the persistent forward, whose CTAs
+    walk several (head, query block) items; ragged last blocks of queries and keys."""
     inp = make_qkv(2, 96, n, 64, seed=7500 + n, with_do=False)
     o, lse = run_fwd(inp, 0.125)
     sel = np.arange(0, 192, 7)   # every 7th head of the 192, in full
