@@ -67,3 +67,50 @@ def test_graph_replay_matches_eager(shape):
         for n_ in ("o", "lse", "dk", "dv"):
             np.testing.assert_array_equal(replay[n_], eager[n_], err_msg=n_)
         np.testing.assert_allclose(replay["dq"], eager["dq"], rtol=2 ** -7, atol=2 ** -12)
+
+
+@pytest.mark.parametrize("shape", [(8, 12, 196, 64), (1, 4, 700, 128)])
+def test_graph_replay_deterministic_bitwise(shape):
+    """The deterministic backward has no atomics: a replayed graph of forward + deterministic
+    backward reproduces eager calls bit for bit, dQ included."""
+    B, H, N, D = shape
+    scale = 1.0 / math.sqrt(D)
+    bufs = {x: torch.empty(B, H, N, D, dtype=torch.bfloat16, device="cuda") for x in ("q", "k", "v", "do")}
+    o, dq, dk, dv = (torch.empty(B, H, N, D, dtype=torch.bfloat16, device="cuda") for _ in range(4))
+    lse = torch.empty(B, H, N, device="cuda")
+    wsb = sa.attn_bwd_workspace_size(B, H, N, D)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+
+    def step(outs):
+        o_, lse_, dq_, dk_, dv_ = outs
+        sa.attn_fwd(bufs["q"], bufs["k"], bufs["v"], o_, lse_, B, H, N, D, scale, s)
+        sa.attn_bwd_deterministic(bufs["q"], bufs["k"], bufs["v"], o_, bufs["do"], lse_, dq_, dk_, dv_,
+                                  ws, wsb, B, H, N, D, scale, s)
+
+    outs = (o, lse, dq, dk, dv)
+    first = make_qkv(B, H, N, D, seed=9400 + N, with_do=True)
+    for x in bufs:
+        bufs[x].copy_(first[x])
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        step(outs)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step(outs)
+    torch.cuda.synchronize()
+    inp = make_qkv(B, H, N, D, seed=9500 + N, with_do=True)
+    for x in bufs:
+        bufs[x].copy_(inp[x])
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    assert sa.attn_get_device_status() == 0
+    replay = [t.float().cpu().numpy() for t in outs]
+    eager_outs = tuple(torch.empty_like(t) for t in outs)
+    with torch.cuda.stream(s):
+        step(eager_outs)
+    torch.cuda.synchronize()
+    for name, a, b in zip(("o", "lse", "dq", "dk", "dv"), replay, (t.float().cpu().numpy() for t in eager_outs)):
+        np.testing.assert_array_equal(a, b, err_msg=name)
