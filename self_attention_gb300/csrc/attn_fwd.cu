@@ -617,16 +617,16 @@ __global__ void __launch_bounds__(192, 2)
 // taken in a grid-stride order by CTAs that stay resident (two per SM), so the loads of the
 // next item, the tail of the previous one and the other CTA's work hide each other's latency.
 //   warp 4      TMA: Q of each item into one of two Q buffers, K/V tiles through one ring that
-//               runs across items.
+//               runs across items; before a Q buffer takes its next Q, the O tile that the
+//               softmax warps staged there leaves with one TMA tensor store (rows past N clipped).
 //   warp 5      tcgen05: S = Q K_j^T, then O += P V_j; as in fwd_sp_kernel the next S, of this
 //               item or the next, is issued as soon as the softmax warps have read S, and runs
 //               under their exponentials.
 //   warps 0-3   softmax as fwd_sp_kernel (P in TMEM columns of its own), then the epilogue of
 //               the item: the normalised bf16 tile goes into the item's Q buffer (free once the
-//               item's last S has read it), in the 128-byte-swizzled layout, and leaves with
-//               one TMA tensor store (rows past N are clipped); the Q buffer returns to the
-//               producer once the store has read it.  The next item's first P V (accumulate
-//               off) follows the softmax warps' next P, after this epilogue has read O.
+//               item's last S has read it), in the 128-byte-swizzled layout, for the producer
+//               to store.  The next item's first P V (accumulate off) follows the softmax warps'
+//               next P, after this epilogue has read O.
 // TMEM columns: S [0,128), O [128,128+d), P [128+d,128+d+64).
 template <int D>
 struct PersistCfg {
@@ -655,7 +655,7 @@ __global__ void __launch_bounds__(192, 2)
     uint8_t *sK = sQ + 2 * C::Q_BYTES;
     uint8_t *sV = sK + C::STAGES * C::KV_BYTES;
 
-    __shared__ uint64_t bar_qf[2], bar_qfree[2];
+    __shared__ uint64_t bar_qf[2], bar_ost[2];   // Q loaded; O staged in the Q buffer
     __shared__ uint64_t bar_kf[C::STAGES], bar_ke[C::STAGES], bar_vf[C::STAGES], bar_ve[C::STAGES];
     __shared__ uint64_t bar_s, bar_sread, bar_p, bar_pv, bar_done;
     __shared__ uint32_t tmem_sh;
@@ -670,7 +670,7 @@ __global__ void __launch_bounds__(192, 2)
         abort_sh = 0;
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(&bar_qf[b], 1);
-            ptx::mbar_init(&bar_qfree[b], 1);
+            ptx::mbar_init(&bar_ost[b], 128);
         }
         for (int s = 0; s < C::STAGES; ++s) {
             ptx::mbar_init(&bar_kf[s], 1);
@@ -700,13 +700,26 @@ __global__ void __launch_bounds__(192, 2)
             ptx::tma_prefetch_desc(&tm_q);
             ptx::tma_prefetch_desc(&tm_k);
             ptx::tma_prefetch_desc(&tm_v);
+            // item li - 2's O, staged in Q buffer li % 2, out to global memory
+            auto store_o = [&](int li) {
+                const int item = first + li * stride;
+                const int bh = item / n_qblocks, q0 = (item % n_qblocks) * C::BM;
+                const int qb = li & 1;
+                wait_bounded(&bar_ost[qb], (li >> 1) & 1, g);
+                for (int h = 0; h < D / 64; ++h)
+                    ptx::tma_store_3d(&tm_o, sQ + qb * C::Q_BYTES + h * C::BM * 128, h * 64, q0, bh);
+                ptx::bulk_commit_group();
+            };
             int kt = 0;   // K/V tiles loaded so far (ring position)
             int li = 0;
             for (int item = first; item < n_items; item += stride, ++li) {
                 const int bh = item / n_qblocks, q0 = (item % n_qblocks) * C::BM;
                 const int qb = li & 1;
-                // Q buffer qb held item li - 2's Q, then its O on the way out
-                wait_bounded(&bar_qfree[qb], ((li >> 1) & 1) ^ 1, g);
+                // Q buffer qb held item li - 2's Q, then its O: store that and let it be read
+                if (li >= 2) {
+                    store_o(li - 2);
+                    ptx::bulk_wait_group_read<0>();
+                }
                 ptx::mbar_arrive_expect_tx(&bar_qf[qb], C::Q_BYTES);
                 for (int h = 0; h < D / 64; ++h)
                     ptx::tma_load_3d(sQ + qb * C::Q_BYTES + h * C::BM * 128, &tm_q, &bar_qf[qb],
@@ -726,6 +739,9 @@ __global__ void __launch_bounds__(192, 2)
                                          h * 64, j * C::BN, bh);
                 }
             }
+            // the last two items' O, then every store complete before the CTA exits
+            for (int l2 = (li > 2 ? li - 2 : 0); l2 < li; ++l2) store_o(l2);
+            ptx::bulk_wait_group<0>();
             // Do not leave the CTA with copies in flight (matters only after a timeout).
             for (int t = (kt > C::STAGES ? kt - C::STAGES : 0); t < kt; ++t) {
                 wait_bounded(&bar_kf[t % C::STAGES], (t / C::STAGES) & 1, g);
@@ -911,19 +927,9 @@ __global__ void __launch_bounds__(192, 2)
             }
             ptx::tc_fence_before();   // O read: the next item's first P V may overwrite it
             ptx::fence_proxy_async_smem();
-            ptx::named_bar(1, 128);
-            if (threadIdx.x == 0) {
-                for (int h = 0; h < D / 64; ++h)
-                    ptx::tma_store_3d(&tm_o, sQ + qb * C::Q_BYTES + h * C::BM * 128, h * 64, q0, bh);
-                ptx::bulk_commit_group();
-                // the Q buffer goes back to the producer (for item li + 2) once the store has
-                // read it out of shared memory
-                ptx::bulk_wait_group_read<0>();
-                ptx::mbar_arrive(&bar_qfree[qb]);
-            }
+            ptx::mbar_arrive(&bar_ost[qb]);   // the producer stores the tile
             if (row < n) lse[(size_t)bh * n + row] = (m + log2f(l)) * kLn2;
         }
-        if (threadIdx.x == 0) ptx::bulk_wait_group<0>();   // stores complete before the CTA exits
     }
 
     ptx::tc_fence_before();
