@@ -64,33 +64,58 @@ struct BwdCfg {
 // probability there), interleaved per pair of rows as {-LSE2_2k, -LSE2_2k+1, -D_2k, -D_2k+1}
 // so that one 16-byte load gives the packed operands for two queries.  Then zero the dQ
 // accumulator.
+// Layout: D / 8 consecutive threads share a row, 16 bytes of O and of dO each; a pass takes
+// kPreRows rows per thread, all loads issued before any is reduced, so that each thread keeps
+// several 16-byte loads in flight.  The padded row index g = h n_pad + i advances by a fixed
+// stride, kept as (h, i) without a division per row.
+constexpr int kPreRows = 4;
+
 template <int D>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 4)
     bwd_preprocess_kernel(const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restrict__ dout,
                           const float *__restrict__ lse, float *__restrict__ stats,
                           float *__restrict__ dq_acc, int bh, int n,
                           int n_pad, int zero_acc)
 {
-    constexpr int TPR = D / 8;  // threads per row, 8 bf16 (16 bytes) each
-    const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    const long long nthreads = (long long)gridDim.x * blockDim.x;
+    constexpr int TPR = D / 8;         // threads per row
+    constexpr int RPW = 32 / TPR;      // rows per warp
+    const int part = threadIdx.x % TPR;
     const long long rows = (long long)bh * n_pad;
-    // Whole warps run the same iterations (nthreads is a multiple of 32), so the shuffles
-    // below always see all 32 lanes.
-    const long long total = rows * TPR;
-    const long long bound = (total + 31) & ~31LL;
-    for (long long t = tid; t < bound; t += nthreads) {
-        const long long prow = t / TPR;
-        const int part = (int)(t % TPR);
-        const int h = (int)(prow / n_pad), i = (int)(prow % n_pad);
-        const bool live = t < total && i < n;
-        const long long row = (long long)h * n + i;
-        float acc = 0.f;
-        if (live) {
-            const uint4 a = *reinterpret_cast<const uint4 *>(o + row * D + part * 8);
-            const uint4 b = *reinterpret_cast<const uint4 *>(dout + row * D + part * 8);
-            const __nv_bfloat162 *a2 = reinterpret_cast<const __nv_bfloat162 *>(&a);
-            const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&b);
+    const long long stride = (long long)gridDim.x * (blockDim.x / TPR);   // rows per step
+    const long long g_first = (long long)blockIdx.x * (blockDim.x / TPR) + threadIdx.x / TPR;
+    // The loop tests the warp's first row, so whole warps run the same passes and the
+    // shuffles below always see all 32 lanes.
+    const long long g_warp = g_first - (threadIdx.x % 32) / TPR;
+    const long long step_h = stride / n_pad;
+    const int step_i = (int)(stride % n_pad);
+    long long h = g_first / n_pad;
+    int i = (int)(g_first % n_pad);
+    for (long long gw = g_warp, g = g_first; gw < rows; gw += kPreRows * stride, g += kPreRows * stride) {
+        uint4 a[kPreRows], b[kPreRows];
+        float l[kPreRows];   // LSE of the row; +inf for a padding row, whose -LSE2 is -inf
+#pragma unroll
+        for (int u = 0; u < kPreRows; ++u) {
+            const bool live = g + u * stride < rows && i < n;
+            const long long row = h * n + i;
+            a[u] = b[u] = make_uint4(0u, 0u, 0u, 0u);
+            l[u] = INFINITY;
+            if (live) {
+                a[u] = *reinterpret_cast<const uint4 *>(o + row * D + part * 8);
+                b[u] = *reinterpret_cast<const uint4 *>(dout + row * D + part * 8);
+                if (part == 0) l[u] = lse[row];
+            }
+            i += step_i;
+            h += step_h;
+            if (i >= n_pad) {
+                i -= n_pad;
+                ++h;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kPreRows; ++u) {
+            const __nv_bfloat162 *a2 = reinterpret_cast<const __nv_bfloat162 *>(&a[u]);
+            const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&b[u]);
+            float acc = 0.f;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const float2 fa = __bfloat1622float2(a2[e]);
@@ -98,16 +123,20 @@ __global__ void __launch_bounds__(256)
                 acc = fmaf(fa.x, fb.x, acc);
                 acc = fmaf(fa.y, fb.y, acc);
             }
-        }
 #pragma unroll
-        for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (t < total && part == 0) {
-            float *pair = stats + (prow >> 1) * 4 + (prow & 1);   // n_pad is even
-            pair[0] = i < n ? -lse[row] * kLog2e : -INFINITY;
-            pair[2] = -acc;
+            for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            const long long prow = g + u * stride;
+            if (prow < rows && part == 0) {
+                float *pair = stats + (prow >> 1) * 4 + (prow & 1);   // n_pad is even
+                pair[0] = -l[u] * kLog2e;
+                pair[2] = -acc;
+            }
         }
     }
+    static_assert(RPW * TPR == 32, "a warp covers whole rows");
     if (!zero_acc) return;
+    const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long nthreads = (long long)gridDim.x * blockDim.x;
     float4 *acc4 = reinterpret_cast<float4 *>(dq_acc);
     const long long n4 = (long long)bh * n * D / 4;
     for (long long t = tid; t < n4; t += nthreads) acc4[t] = make_float4(0.f, 0.f, 0.f, 0.f);
