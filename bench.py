@@ -39,6 +39,7 @@ PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "bwd_main_long_text.md")
 KERNEL_SOURCES = [os.path.join(ROOT, "self_attention_gb300", "csrc", f)
                   for f in ("attn_bwd.cu", "common.cuh", "ptx.cuh")]
 # Peaks used when the measured-peaks file is absent (one earlier GB300 measurement).
+L2_BYTES = 129e6   # GB300 L2 capacity
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -357,6 +358,11 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     if sa.attn_get_device_status() != 0:
         raise RuntimeError("device status reported a kernel timeout during warm-up")
+    # Inputs that fit in L2 would stay there from one step to the next: then a buffer larger
+    # than L2 is written before each timed step, outside that step's events, and the step time
+    # is the mean of the per-step event intervals.
+    in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, do))
+    l2_flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda") if in_bytes < L2_BYTES else None
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -370,6 +376,8 @@ def run_ours(args, world, rank, local):
     time.sleep(0.3)
     start.record(stream)
     for i in range(args.steps):
+        if l2_flush is not None:
+            l2_flush.fill_(i & 0xff)
         step(evs[i])
     stop.record(stream)
     torch.cuda.synchronize()
@@ -381,7 +389,8 @@ def run_ours(args, world, rank, local):
 
     ms = lambda a, b: a.elapsed_time(b)
     local_res = {
-        "step_ms": ms(start, stop) / args.steps,
+        "step_ms": (ms(start, stop) / args.steps if l2_flush is None
+                    else statistics.mean(ms(e[0], e[4]) for e in evs)),
         "fwd_ms": statistics.mean(ms(e[0], e[1]) for e in evs),
         "bwd_ms": statistics.mean(ms(e[1], e[4]) for e in evs),
         "bwd_main_ms": statistics.mean(ms(e[2], e[3]) for e in evs),
@@ -535,8 +544,12 @@ def run_ours(args, world, rank, local):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "B": B, "H": H, "N": N, "d_k": D, "seq_len": N,
                    "global_batch": B * world, "parallelism": f"independent batches x{world}",
-                   "qk_std": w.qk_std, "l2": "no flush: inputs (Q,K,V,dO = "
-                   f"{h2d / 1e6:.0f} MB) are larger than the 129 MB L2"},
+                   "qk_std": w.qk_std,
+                   "l2": (f"no flush: inputs (Q,K,V,dO = {in_bytes / 1e6:.0f} MB) are larger than the "
+                          f"{L2_BYTES / 1e6:.0f} MB L2" if l2_flush is None else
+                          f"flushed: inputs (Q,K,V,dO = {in_bytes / 1e6:.0f} MB) fit the "
+                          f"{L2_BYTES / 1e6:.0f} MB L2, so a 256 MB buffer is written before each "
+                          "timed step, outside its events")},
         "fwd_tflops": per_gpu_fwd, "bwd_tflops": per_gpu_bwd,
         "fwd_pct_of_bf16_peak": 100.0 * per_gpu_fwd / peaks["bf16_tflops"],
         "bwd_pct_of_bf16_peak": 100.0 * per_gpu_bwd / peaks["bf16_tflops"],
