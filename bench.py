@@ -38,8 +38,8 @@ UNIT = "TFLOPS"
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "bwd_main_long_text.md")
 KERNEL_SOURCES = [os.path.join(ROOT, "self_attention_gb300", "csrc", f)
                   for f in ("attn_bwd.cu", "common.cuh", "ptx.cuh")]
-# Peaks used when the measured-peaks file is absent (one earlier GB300 measurement).
 L2_BYTES = 129e6   # GB300 L2 capacity
+# Peaks used when the measured-peaks file is absent (one earlier GB300 measurement).
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
