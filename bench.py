@@ -397,6 +397,25 @@ def run_ours(args, world, rank, local):
         "flops": (4.0 + 10.0) * B * H * N * N * D,
     }
 
+    # The deterministic backward (attn_bwd_deterministic: preprocess, the dK / dV pass and the
+    # query-stationary dQ pass, no atomics) on the same inputs, outside the timed region above:
+    # warm-up, then CUDA events around each call, with the L2 flush as above where the inputs
+    # fit in L2.
+    det_iters = max(1, min(10, args.steps))
+    sa.attn_bwd_deterministic(q, k, v, o, do, lse, dq, dk, dv, ws, ws_bytes, B, H, N, D, scale, stream)
+    det_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(det_iters)]
+    for i in range(det_iters):
+        if l2_flush is not None:
+            l2_flush.fill_(i & 0xff)
+        det_evs[i][0].record(stream)
+        sa.attn_bwd_deterministic(q, k, v, o, do, lse, dq, dk, dv, ws, ws_bytes, B, H, N, D, scale, stream)
+        det_evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    if sa.attn_get_device_status() != 0:
+        raise RuntimeError("device status reported a kernel timeout in the deterministic backward")
+    det_ms = statistics.mean(ms(a, b) for a, b in det_evs)
+
     # End to end through the C-ABI calls: every step copies its inputs from pinned host memory
     # to the device, runs attn_fwd and attn_bwd, and copies all outputs (O, LSE, dQ, dK, dV)
     # back to pinned host memory, all inside the timed region.  The steps are pipelined the way
@@ -562,6 +581,12 @@ def run_ours(args, world, rank, local):
         "cpu_baseline": cpu,
         "qkv_proj": {"workload": "vit_b_mhsa_block X [32, 576, 768] x 3 W [768, 768], 12 heads",
                      **proj},
+        "deterministic_bwd": {
+            "call": "attn_bwd_deterministic (preprocess, dK/dV pass, query-stationary dQ pass; "
+                    "no atomics, bitwise reproducible)",
+            "ms": det_ms, "tflops": 10.0 * B * H * N * N * D / (det_ms * 1e-3) / 1e12,
+            "atomic_bwd_ms": local_res["bwd_ms"], "time_vs_atomic": det_ms / local_res["bwd_ms"],
+            "calls": det_iters},
         "configs": configs,
         "hbm_probe": {"kernel": "vector_add (fp32, 3 x 512 MiB)", "gbs": probe_gbs,
                       "frac_of_measured_copy": probe_gbs / peaks["hbm_gbs"]},
