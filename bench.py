@@ -182,21 +182,55 @@ def oracle_sample(w, tokens: int):
     return {x: sl(inp[x]) for x in ("q", "k", "v", "do")}, s
 
 
-def time_oracle(w, tokens: int, repeats: int):
+def time_oracle(w, tokens: int, repeats: int, outputs: dict | None = None):
+    """Wall times of the oracle's forward + backward on the sample; `outputs`, if given, receives
+    the sample and the last run's results."""
     import oracle
     sample, s = oracle_sample(w, tokens)
     oracle.build()
     times = []
     for _ in range(repeats):
         t0 = time.perf_counter()
-        oracle.fwd(sample["q"], sample["k"], sample["v"], w.scale)
-        oracle.bwd(sample["q"], sample["k"], sample["v"], sample["do"], w.scale)
+        fwd = oracle.fwd(sample["q"], sample["k"], sample["v"], w.scale)
+        bwd = oracle.bwd(sample["q"], sample["k"], sample["v"], sample["do"], w.scale)
         times.append(time.perf_counter() - t0)
+    if outputs is not None:
+        outputs.update(sample=sample, o=fwd[0], lse=fwd[1], dq=bwd["dq"], dk=bwd["dk"], dv=bwd["dv"])
     flops = 14.0 * s * s * w.d
     cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
     desc = (f"oracle fwd+bwd (fp64, N x N materialised) on one head of {w.name}: its first {s} "
             f"tokens, d_k={w.d}; {14 * s * s * w.d:.3g} metric flops per run")
     return times, flops, cores, desc
+
+
+def error_norms(got: dict, ref: dict) -> dict:
+    """GPU results against the oracle's fp64 ones (numpy arrays keyed o, lse, dq, dk, dv): O max
+    abs and relative Frobenius error, LSE relative error, the gradients' relative Frobenius
+    errors.  The stated bounds are 1e-2, 5e-3, 1e-4 and 1e-2, with the O bound read as the bf16
+    rounding floor where that exceeds 1e-2 (|O| >= 2, where one bf16 step is 2^-6 or more), so
+    the O error is also given in bf16 steps of the reference value at its largest element."""
+    import numpy as np
+    rel_fro = lambda x: float(np.linalg.norm(got[x] - ref[x]) / max(np.linalg.norm(ref[x]), 1e-300))
+    err = np.abs(got["o"] - ref["o"]).ravel()
+    i = int(err.argmax())
+    r_i = abs(float(ref["o"].ravel()[i]))
+    step = 2.0 ** (math.floor(math.log2(max(r_i, 2.0 ** -126))) - 7)   # bf16: 8 significant bits
+    return {"o_max_abs": float(err[i]), "o_ref_at_max": r_i, "o_max_abs_in_bf16_steps": float(err[i]) / step,
+            "o_elems_over_1e-2": int((err > 1e-2).sum()), "o_rel_fro": rel_fro("o"),
+            "lse_rel": float(np.abs(got["lse"] - ref["lse"]).max() / max(np.abs(ref["lse"]).max(), 1.0)),
+            "dq_rel_fro": rel_fro("dq"), "dk_rel_fro": rel_fro("dk"), "dv_rel_fro": rel_fro("dv")}
+
+
+def sample_parity(sa, w, ref: dict, stream) -> dict:
+    """The GPU path (attn_fwd, attn_bwd) on the oracle's sample, against the oracle's results."""
+    import torch
+    q, k, v, do = (ref["sample"][x].cuda() for x in ("q", "k", "v", "do"))
+    o, lse = sa.forward(q, k, v, w.scale, stream)
+    dq, dk, dv = sa.backward(q, k, v, o, do, lse, w.scale, stream)
+    torch.cuda.synchronize()
+    got = {name: t.double().cpu().numpy() for name, t in
+           (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+    return error_norms(got, ref)
 
 
 def run_reference(args, world, rank):
@@ -553,9 +587,11 @@ def run_ours(args, world, rank, local):
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        times, oflops, cores, desc = time_oracle(w, args.cpu_baseline_tokens, 1)
+        ref = {}
+        times, oflops, cores, desc = time_oracle(w, args.cpu_baseline_tokens, 1, outputs=ref)
         cpu = {"value": oflops / times[0] / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": desc + f"; wall {times[0]:.2f} s"}
+               "sample": desc + f"; wall {times[0]:.2f} s",
+               "gpu_errors_on_sample": sample_parity(sa, w, ref, stream)}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -594,6 +630,8 @@ def run_ours(args, world, rank, local):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,
+        "system": {"gpu": torch.cuda.get_device_name(local), "torch": torch.__version__,
+                   "cuda": torch.version.cuda, "sm_count": props.multi_processor_count},
     }
     print(json.dumps(line), flush=True)
     if world > 1:

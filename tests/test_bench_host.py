@@ -94,3 +94,25 @@ def test_default_run_is_the_long_text_workload_with_enough_warmup():
     assert (w.name, w.B, w.H, w.N, w.d) == ("long_text", 2, 16, 16384, 128)
     w = bench.workload(bench.parse_args(["--workload", "vit_b16_batch", "--shape", "1,16,8192,128"]))
     assert (w.B, w.H, w.N, w.d) == (1, 16, 8192, 128) and w.name.startswith("vit_b16_batch")
+
+
+def test_error_norms_of_the_sample_check():
+    np = pytest.importorskip("numpy")
+    rng = np.random.default_rng(5)
+    ref = {"o": rng.normal(size=(1, 1, 40, 8)), "lse": rng.normal(size=(1, 1, 40)) + 3.0,
+           "dq": rng.normal(size=(1, 1, 40, 8)), "dk": rng.normal(size=(1, 1, 40, 8)),
+           "dv": rng.normal(size=(1, 1, 40, 8))}
+    ref["o"][0, 0, 7, 3] = 3.0                       # one large output, where a bf16 step is 2^-6
+    got = {k: v.copy() for k, v in ref.items()}
+    got["o"][0, 0, 7, 3] += 2.0 ** -6                # exactly one step off there
+    got["o"][0, 0, 1, 1] += 1e-3
+    got["lse"][0, 0, 2] += 4e-5 * 4.0
+    got["dq"] *= 1.004
+    e = bench.error_norms(got, ref)
+    assert e["o_max_abs"] == pytest.approx(2.0 ** -6) and e["o_ref_at_max"] == 3.0
+    assert e["o_max_abs_in_bf16_steps"] == pytest.approx(1.0)
+    assert e["o_elems_over_1e-2"] == 1
+    assert e["lse_rel"] == pytest.approx(4e-5 * 4.0 / np.abs(ref["lse"]).max())
+    assert e["dq_rel_fro"] == pytest.approx(0.004)
+    assert e["dk_rel_fro"] == 0.0 and e["dv_rel_fro"] == 0.0
+    assert 0 < e["o_rel_fro"] < 1e-2
