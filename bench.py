@@ -233,6 +233,13 @@ def sample_parity(sa, w, ref: dict, stream) -> dict:
     return error_norms(got, ref)
 
 
+def workload_config(w, world: int) -> dict:
+    """The `config` keys both arms report for a workload run on `world` GPUs (one batch each)."""
+    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d_k": w.d, "seq_len": w.N,
+            "global_batch": w.B * world, "parallelism": f"independent batches x{world}",
+            "qk_std": w.qk_std}
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return 0
@@ -247,8 +254,7 @@ def run_reference(args, world, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d_k": w.d,
-                   "seq_len": w.N, "global_batch": w.B},
+        "config": workload_config(w, world),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -597,9 +603,7 @@ def run_ours(args, world, rank, local):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": res["step_ms"], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "B": B, "H": H, "N": N, "d_k": D, "seq_len": N,
-                   "global_batch": B * world, "parallelism": f"independent batches x{world}",
-                   "qk_std": w.qk_std,
+        "config": {**workload_config(w, world),
                    "l2": (f"no flush: inputs (Q,K,V,dO = {in_bytes / 1e6:.0f} MB) are larger than the "
                           f"{L2_BYTES / 1e6:.0f} MB L2" if l2_flush is None else
                           f"flushed: inputs (Q,K,V,dO = {in_bytes / 1e6:.0f} MB) fit the "

@@ -116,3 +116,10 @@ def test_error_norms_of_the_sample_check():
     assert e["dq_rel_fro"] == pytest.approx(0.004)
     assert e["dk_rel_fro"] == 0.0 and e["dv_rel_fro"] == 0.0
     assert 0 < e["o_rel_fro"] < 1e-2
+
+
+def test_both_arms_describe_the_workload_alike():
+    w = bench.workload(bench.parse_args([]))
+    c = bench.workload_config(w, 4)
+    assert c == {"workload": "long_text", "B": 2, "H": 16, "N": 16384, "d_k": 128, "seq_len": 16384,
+                 "global_batch": 8, "parallelism": "independent batches x4", "qk_std": 2.0}
