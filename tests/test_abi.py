@@ -117,3 +117,29 @@ def test_vector_add_argument_errors(lib):
     assert lib.vector_add(0, K, V, 16, None) == 1
     assert lib.vector_add(Q + 4, K, V, 16, None) == 3
     assert lib.vector_add(Q, K, Q + 16, 16, None) == 1    # partial overlap with an input
+
+
+def test_noalloc_and_deterministic_argument_errors(lib):
+    """attn_bwd_noalloc checks the sizes and its fixed 64 MiB scratch, and
+    attn_bwd_deterministic the same arguments as attn_bwd, before either touches the device."""
+    z = [0] * 9
+    assert lib.attn_bwd_workspace_size(2, 16, 16384, 128) > 64 << 20
+    assert lib.attn_bwd_noalloc(*z, 2, 16, 16384, 128, ctypes.c_float(0.088), None) == 8
+    assert lib.attn_bwd_noalloc(*z, 1, 2, 64, 80, ctypes.c_float(0.125), None) == 2
+    assert lib.attn_bwd_noalloc(*z, 0, 2, 64, 64, ctypes.c_float(0.125), None) == 1
+    assert lib.attn_bwd_noalloc(*z, 1, 2, 64, 64, ctypes.c_float(float("nan")), None) == 1
+
+    ws = 0x70000000
+    need = sa.attn_bwd_workspace_size(1, 2, 64, 64)
+    dq, dk, dv = 0x80000000, 0x90000000, 0xA0000000
+
+    def det(ws=ws, nbytes=need, d=64, dq=dq, dk=dk):
+        return lib.attn_bwd_deterministic(Q, K, V, O, 0x60000000, L, dq, dk, dv, ws, nbytes, 1, 2, 64,
+                                          d, ctypes.c_float(0.125), None)
+
+    assert det(d=96) == 2
+    assert det(nbytes=need - 1) == 6
+    assert det(ws=ws + 64) == 6
+    assert det(dq=K) == 1            # an output aliasing an input
+    assert det(dk=dq) == 1           # two outputs overlapping
+    assert det(dq=dq + 8) == 3
