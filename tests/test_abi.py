@@ -143,3 +143,42 @@ def test_noalloc_and_deterministic_argument_errors(lib):
     assert det(dq=K) == 1            # an output aliasing an input
     assert det(dk=dq) == 1           # two outputs overlapping
     assert det(dq=dq + 8) == 3
+
+
+def test_qkv_proj_argument_errors(lib):
+    """The projection calls check sizes, pointers, alignment and overlaps before the device."""
+    X = 0x10000000                                   # [1, 8, 256] bf16: 4 KB
+    W = (0x20000000, 0x21000000, 0x22000000)         # [256, 256] bf16: 128 KB each
+    OUT = (0x30000000, 0x31000000, 0x32000000)
+
+    def fwd(B=1, N=8, D=256, H=4, d=64, x=X, w=W, o=OUT):
+        return lib.attn_qkv_proj(x, *w, *o, B, N, D, H, d, None)
+
+    assert fwd(d=32) == 2
+    assert fwd(H=3) == 1                             # D != H * d_k
+    assert fwd(D=192, H=3) == 1                      # D not a multiple of 128
+    assert fwd(B=0) == 1
+    assert fwd(x=0) == 1
+    assert fwd(w=(W[0], 0, W[2])) == 1
+    assert fwd(x=X + 8) == 3
+    assert fwd(o=(OUT[0], 0, OUT[2])) == 1
+    assert fwd(o=(OUT[0] + 2, OUT[1], OUT[2])) == 3
+    assert fwd(o=(X, OUT[1], OUT[2])) == 1           # an output over the input
+    assert fwd(o=(OUT[0], W[1], OUT[2])) == 1        # an output over a weight
+    assert fwd(o=(OUT[0], OUT[0] + 16, OUT[2])) == 1  # two outputs overlapping
+
+    DY = (0x60000000, 0x61000000, 0x62000000)
+    DW = (0x50000000, 0x51000000, 0x52000000)        # [256, 256] fp32: 256 KB each
+
+    def bwd(dx=0x40000000, dw=DW, dy=DY, d=64):
+        return lib.attn_qkv_proj_bwd(X, *W, *dy, dx, *dw, 1, 8, 256, 4, d, None)
+
+    assert bwd(d=96) == 2
+    assert bwd(dx=0) == 1
+    assert bwd(dx=0x40000008) == 3
+    assert bwd(dy=(DY[0], DY[1], 0)) == 1
+    assert bwd(dw=(DW[0], 0, DW[2])) == 1
+    assert bwd(dw=(DW[0] + 4, DW[1], DW[2])) == 3
+    assert bwd(dx=X) == 1                            # dX over X
+    assert bwd(dw=(DY[1], DW[1], DW[2])) == 1        # a dW over an incoming gradient
+    assert bwd(dw=(DW[0], DW[0] + 1024, DW[2])) == 1  # two dW overlapping
