@@ -158,6 +158,7 @@ extern "C" attn_status attn_fwd(const void *q, const void *k, const void *v, voi
         (r = make_map(&a.tm_v, v, (int)bh, N, d_k, 128)) != CUDA_SUCCESS ||
         (r = make_map(&a.tm_o, o, (int)bh, N, d_k, 128)) != CUDA_SUCCESS)
         return fail_driver("cuTensorMapEncodeTiled", r);
+    a.v = v;
     a.o = o;
     a.lse = lse;
     a.bh = (int)bh;

@@ -14,15 +14,20 @@
 // used for d = 128 with NQ = 2, shown here.  d = 64, where the softmax work per tile equals the
 // matrix work, runs one tile per CTA and two CTAs per SM: fwd_persistent_kernel, or
 // fwd_sp_kernel where there are fewer tiles than resident CTAs, below):
-//   warp 8      TMA producer: Q tiles once, then a ring of K and V tiles (128 keys each).
+//   warp 8      TMA producer: Q tiles once, then a ring of K tiles and a ring of V tiles (128
+//               keys each).
+//   warps 10-11 V converters: each V tile rewritten as fp16 in shared memory once it has landed.
 //   warp 9      tcgen05 issuer: S_t = Q_t K_j^T into TMEM (fp32), then O_t += P_t V_j with
-//               P_t read from TMEM (bf16, written over S_t) and V_j from shared memory.
+//               P_t read from TMEM (fp16, written over S_t) and V_j (fp16) from shared memory.
 //   warps 0-7   two softmax warpgroups, one per query tile; thread = one query row.  They
 //               read S_t from TMEM, update the running max m (log2 units, scale folded into
-//               log2 e) and sum l, write P_t = 2^(x - m) as bf16 back into TMEM and rescale
+//               log2 e) and sum l, write P_t = 2^(x - m) as fp16 back into TMEM and rescale
 //               O_t in TMEM when the maximum grew by more than kTau (exact: the final
 //               division uses the same m).  The two tiles alternate on the tensor core, so
 //               one tile's softmax overlaps the other tile's matrix products.
+// P V runs in fp16 rather than bf16 (the two operands of one MMA share their type): an fp16
+// weight is off by at most 2^-11 of itself where a bf16 one is off by 2^-8, and V's bf16 values
+// are exact in fp16 across fp16's normal range.
 // TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+d), O_1 [256+d,256+2d).
 #include <algorithm>
 
@@ -37,6 +42,35 @@ constexpr float kLn2 = 0.6931471805599453f;
 // The running maximum is only moved (and O rescaled) when a tile raises it by more than this
 // many powers of two; in between, probabilities may reach 2^kTau, far from fp32/bf16 limits.
 constexpr float kTau = 8.0f;
+// P = 2^(x - m + kPOff) enters P V as fp16: with the maximum lagging by at most kTau the
+// largest weight is 2^(kTau + kPOff) = 2^15, inside fp16's range, and the offset keeps weights
+// down to 2^-31 of the row maximum out of fp16's flush-to-zero.  The row sum l adds the weights
+// in fp32 before they are rounded; the offset cancels in O = acc / l, and LSE subtracts it.
+constexpr float kPOff = 7.0f;
+
+// Rewrites a shared tile of bf16 pairs as fp16 pairs, in place, 16 bytes at a time (the tile's
+// swizzle permutes whole 16-byte chunks, so it is untouched): the NT calling threads take chunks
+// ct, ct + NT, ... of the CHUNKS at `base`, PASS chunks per thread at a time with all of a pass's
+// loads issued before its stores.  Rounding bf16 to fp16 is exact for magnitudes in fp16's
+// normal range [2^-14, 65504]; smaller ones round to fp16's subnormal grid of 2^-24, larger ones
+// become infinite.
+template <int CHUNKS, int NT, int PASS>
+__device__ __forceinline__ void tile_bf16_to_f16(uint32_t base, int ct)
+{
+    constexpr int PER_THREAD = CHUNKS / NT;
+    static_assert(CHUNKS % NT == 0 && PER_THREAD % PASS == 0, "whole passes");
+#pragma unroll 1
+    for (int p = 0; p < PER_THREAD / PASS; ++p) {
+        uint4 v[PASS];
+#pragma unroll
+        for (int k = 0; k < PASS; ++k) v[k] = lds_u128(base + (uint32_t)(ct + NT * (PASS * p + k)) * 16u);
+#pragma unroll
+        for (int k = 0; k < PASS; ++k)
+            sts_u128(base + (uint32_t)(ct + NT * (PASS * p + k)) * 16u,
+                     make_uint4(ptx::bf16x2_to_f16x2(v[k].x), ptx::bf16x2_to_f16x2(v[k].y),
+                                ptx::bf16x2_to_f16x2(v[k].z), ptx::bf16x2_to_f16x2(v[k].w)));
+    }
+}
 
 template <int D, int NQ_>
 struct FwdCfg {
@@ -45,12 +79,17 @@ struct FwdCfg {
     static constexpr int BN = 128;  // keys per K/V tile
     // One tile per CTA (short sequences) keeps shared memory and TMEM small enough for two
     // CTAs per SM, which then hide each other's load and epilogue latency.
-    static constexpr int STAGES = NQ == 1 ? 2 : (D == 64) ? 4 : 2;
+    static constexpr int STAGES = NQ == 1 ? 2 : (D == 64) ? 4 : 2;   // K ring
+    // V ring: one stage deeper than the K ring, so that each V tile has landed, and has been
+    // rewritten as fp16, well before its P V
+    static constexpr int VSTAGES = STAGES + 1;
     static constexpr int Q_BYTES = BM * D * 2;
     static constexpr int KV_BYTES = BN * D * 2;
-    static constexpr int SMEM_BYTES = NQ * Q_BYTES + 2 * STAGES * KV_BYTES + 1024;
-    static constexpr int TMA_WARP = 4 * NQ, MMA_WARP = 4 * NQ + 1;
-    static constexpr int THREADS = 32 * (4 * NQ + 2);
+    static constexpr int SMEM_BYTES = NQ * Q_BYTES + (STAGES + VSTAGES) * KV_BYTES + 1024;
+    static_assert(SMEM_BYTES <= 227 * 1024 - 512, "dynamic + static shared memory over 227 KB");
+    static constexpr int TMA_WARP = 4 * NQ, MMA_WARP = 4 * NQ + 1, CONV_WARP = 4 * NQ + 2;
+    static constexpr int CONV_THREADS = 64, CONV_PASS = 16;   // 16 loads in flight per thread
+    static constexpr int THREADS = 32 * (4 * NQ + 4);
     static constexpr uint32_t TM_O = NQ * 128;  // first O column
     static constexpr uint32_t TM_COLS = NQ == 1 ? 256 : 512;
     static constexpr int MIN_BLOCKS = NQ == 1 ? 2 : 1;
@@ -70,7 +109,8 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::THREADS, FwdCfg<D, NQ>::MIN_BLO
     uint8_t *sV = sK + C::STAGES * C::KV_BYTES;
 
     __shared__ uint64_t bar_q;
-    __shared__ uint64_t bar_kf[C::STAGES], bar_ke[C::STAGES], bar_vf[C::STAGES], bar_ve[C::STAGES];
+    __shared__ uint64_t bar_kf[C::STAGES], bar_ke[C::STAGES];
+    __shared__ uint64_t bar_vf[C::VSTAGES], bar_ve[C::VSTAGES], bar_vc[C::VSTAGES];   // vc: V as fp16
     __shared__ uint64_t bar_s[2], bar_p[2], bar_o[2], bar_done;
     __shared__ uint32_t tmem_sh;
     __shared__ int abort_sh;
@@ -87,8 +127,11 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::THREADS, FwdCfg<D, NQ>::MIN_BLO
         for (int s = 0; s < C::STAGES; ++s) {
             ptx::mbar_init(&bar_kf[s], 1);
             ptx::mbar_init(&bar_ke[s], 1);
+        }
+        for (int s = 0; s < C::VSTAGES; ++s) {
             ptx::mbar_init(&bar_vf[s], 1);
             ptx::mbar_init(&bar_ve[s], 1);
+            ptx::mbar_init(&bar_vc[s], C::CONV_THREADS);
         }
         for (int t = 0; t < C::NQ; ++t) {
             ptx::mbar_init(&bar_s[t], 1);
@@ -126,25 +169,24 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::THREADS, FwdCfg<D, NQ>::MIN_BLO
                 for (int h = 0; h < D / 64; ++h)
                     ptx::tma_load_3d(sK + s * C::KV_BYTES + h * C::BN * 128, &tm_k, &bar_kf[s],
                                      h * 64, j * C::BN, bh);
-                wait_bounded(&bar_ve[s], ph ^ 1, g);
-                ptx::mbar_arrive_expect_tx(&bar_vf[s], C::KV_BYTES);
+                const int sv = j % C::VSTAGES;
+                wait_bounded(&bar_ve[sv], ((j / C::VSTAGES) & 1) ^ 1, g);
+                ptx::mbar_arrive_expect_tx(&bar_vf[sv], C::KV_BYTES);
                 for (int h = 0; h < D / 64; ++h)
-                    ptx::tma_load_3d(sV + s * C::KV_BYTES + h * C::BN * 128, &tm_v, &bar_vf[s],
+                    ptx::tma_load_3d(sV + sv * C::KV_BYTES + h * C::BN * 128, &tm_v, &bar_vf[sv],
                                      h * 64, j * C::BN, bh);
             }
             // Do not leave the CTA with copies in flight (matters only after a timeout).
-            for (int j = (nkv > C::STAGES ? nkv - C::STAGES : 0); j < nkv; ++j) {
-                const int s = j % C::STAGES;
-                const uint32_t ph = (j / C::STAGES) & 1;
-                wait_bounded(&bar_kf[s], ph, g);
-                wait_bounded(&bar_vf[s], ph, g);
-            }
+            for (int j = (nkv > C::STAGES ? nkv - C::STAGES : 0); j < nkv; ++j)
+                wait_bounded(&bar_kf[j % C::STAGES], (j / C::STAGES) & 1, g);
+            for (int j = (nkv > C::VSTAGES ? nkv - C::VSTAGES : 0); j < nkv; ++j)
+                wait_bounded(&bar_vf[j % C::VSTAGES], (j / C::VSTAGES) & 1, g);
         }
     } else if (warp == C::MMA_WARP) {
         // ---------------------------------------------------------------- MMA issuer
         if (ptx::elect_one()) {
             const uint32_t idS = ptx::idesc_bf16_f32(128, C::BN, false, false);
-            const uint32_t idO = ptx::idesc_bf16_f32(128, D, false, true);
+            const uint32_t idO = ptx::idesc_f16_f32(128, D, false, true);
             const uint32_t q_base = ptx::smem_u32(sQ), k_base = ptx::smem_u32(sK),
                            v_base = ptx::smem_u32(sV);
             // S_t = Q_t K^T: both operands K-major (d contiguous), 64-column halves for d=128.
@@ -157,12 +199,13 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::THREADS, FwdCfg<D, NQ>::MIN_BLO
                     ptx::mma_ss(tmem + t * 128, a, b, idS, kk > 0 ? 1u : 0u);
                 }
             };
-            // O_t += P_t V: P from TMEM (8 columns = 16 keys per step), V MN-major (d contiguous).
-            auto issue_pv = [&](int t, int s, bool acc) {
+            // O_t += P_t V: fp16 P from TMEM (8 columns = 16 keys per step), fp16 V MN-major (d
+            // contiguous).
+            auto issue_pv = [&](int t, int sv, bool acc) {
 #pragma unroll
                 for (int kk = 0; kk < C::BN / 16; ++kk) {
                     const uint64_t b =
-                        ptx::sdesc_sw128(v_base + s * C::KV_BYTES + kk * 2048, C::BN * 128, 1024);
+                        ptx::sdesc_sw128(v_base + sv * C::KV_BYTES + kk * 2048, C::BN * 128, 1024);
                     ptx::mma_ts(tmem + C::TM_O + t * D, tmem + t * 128 + kk * 8, b, idO,
                                 (acc || kk > 0) ? 1u : 0u);
                 }
@@ -186,13 +229,14 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::THREADS, FwdCfg<D, NQ>::MIN_BLO
                 const int jn = j + 1;
                 const int sn = jn % C::STAGES;
                 const uint32_t phn = (jn / C::STAGES) & 1;
-                wait_bounded(&bar_vf[s], ph, g);
+                const int sv = j % C::VSTAGES;
+                wait_bounded(&bar_vc[sv], (j / C::VSTAGES) & 1, g);
 #pragma unroll
                 for (int t = 0; t < C::NQ; ++t) {
                     wait_bounded(&bar_p[t], j & 1, g);
                     ptx::tc_fence_after();
-                    issue_pv(t, s, j > 0);
-                    if (t == C::NQ - 1) ptx::mma_commit(&bar_ve[s]);
+                    issue_pv(t, sv, j > 0);
+                    if (t == C::NQ - 1) ptx::mma_commit(&bar_ve[sv]);
                     if (jn < nkv) {
                         if (t == 0) {
                             wait_bounded(&bar_kf[sn], phn, g);
@@ -209,6 +253,17 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::THREADS, FwdCfg<D, NQ>::MIN_BLO
             // Every MMA must have finished before TMEM is released (matters after a timeout).
             ptx::mma_commit(&bar_done);
             wait_bounded(&bar_done, 0, g);
+        }
+    } else if (warp >= C::CONV_WARP) {
+        // ---------------------------------------------------------------- V to fp16
+        // each V tile rewritten as fp16 in place as soon as it has landed
+        const int ct = (warp - C::CONV_WARP) * 32 + lane;
+        for (int j = 0; j < nkv; ++j) {
+            const int sv = j % C::VSTAGES;
+            wait_bounded(&bar_vf[sv], (j / C::VSTAGES) & 1, g);
+            tile_bf16_to_f16<C::KV_BYTES / 16, C::CONV_THREADS, C::CONV_PASS>(ptx::smem_u32(sV + sv * C::KV_BYTES), ct);
+            ptx::fence_proxy_async_smem();
+            ptx::mbar_arrive(&bar_vc[sv]);
         }
     } else {
         // ---------------------------------------------------------------- softmax warpgroups
@@ -255,12 +310,12 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::THREADS, FwdCfg<D, NQ>::MIN_BLO
                 alpha = ptx::ex2(m - m_new);
                 rescale = true;
             }
-            const float neg_m = -m_new;
-            // x c - m for two scores per instruction (f32x2), 2^(.) on the MUFU, the row sum
-            // again two lanes at a time
+            const float neg_m = kPOff - m_new;
+            // x c - m + kPOff for two scores per instruction (f32x2), 2^(.) on the MUFU, the row
+            // sum two lanes at a time in fp32, then the weights rounded to fp16 pairs for P V
             const uint64_t c2 = ptx::f2_pack(scale_log2, scale_log2), nm2 = ptx::f2_pack(neg_m, neg_m);
-            uint64_t acc2[2] = {ptx::f2_pack(0.f, 0.f), ptx::f2_pack(0.f, 0.f)};
-            // P = 2^(x - m) as bf16 pairs into TMEM over S_t, 32 keys (16 columns) at a time
+            uint64_t sum2[2] = {ptx::f2_pack(0.f, 0.f), ptx::f2_pack(0.f, 0.f)};
+            // P as fp16 pairs into TMEM over S_t, 32 keys (16 columns) at a time
 #pragma unroll
             for (int ch = 0; ch < 4; ++ch) {
                 uint32_t pk[16];
@@ -271,14 +326,15 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::THREADS, FwdCfg<D, NQ>::MIN_BLO
                     float t0, t1;
                     ptx::f2_unpack(t, t0, t1);
                     const float p0 = ptx::ex2(t0), p1 = ptx::ex2(t1);
-                    acc2[(i >> 1) & 1] = ptx::add_f32x2(acc2[(i >> 1) & 1], ptx::f2_pack(p0, p1));
-                    pk[i >> 1] = ptx::pack_bf16x2(p0, p1);
+                    sum2[(i >> 1) & 1] = ptx::add_f32x2(sum2[(i >> 1) & 1], ptx::f2_pack(p0, p1));
+                    const uint32_t h = ptx::pack_f16x2(p0, p1);
+                    pk[i >> 1] = h;
                 }
                 ptx::tmem_st16(tS + ch * 16, pk);
             }
             float sum[4];
-            ptx::f2_unpack(acc2[0], sum[0], sum[1]);
-            ptx::f2_unpack(acc2[1], sum[2], sum[3]);
+            ptx::f2_unpack(sum2[0], sum[0], sum[1]);
+            ptx::f2_unpack(sum2[1], sum[2], sum[3]);
             l = l * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
             m = m_new;
             if (rescale) {
@@ -298,7 +354,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::THREADS, FwdCfg<D, NQ>::MIN_BLO
             ptx::mbar_arrive(&bar_p[t]);
         }
 
-        // epilogue: O = O_acc / l (bf16), LSE = (m + log2 l) ln 2
+        // epilogue: O = O_acc / l (bf16), LSE = (m - kPOff + log2 l) ln 2
         wait_bounded(&bar_o[t], 0, g);
         ptx::tc_fence_after();
         const float inv_l = 1.f / l;
@@ -321,7 +377,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::THREADS, FwdCfg<D, NQ>::MIN_BLO
                     dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
             }
         }
-        if (row < n) lse[(size_t)bh * n + row] = (m + log2f(l)) * kLn2;
+        if (row < n) lse[(size_t)bh * n + row] = (m - kPOff + log2f(l)) * kLn2;
     }
 
     ptx::tc_fence_before();
@@ -339,8 +395,10 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::THREADS, FwdCfg<D, NQ>::MIN_BLO
 //   warp 4      TMA producer: Q once, then a ring of K and V tiles.
 //   warp 5      tcgen05 issuer: S_{j+1} = Q K_{j+1}^T once S_j has been read, O += P_j V_j once
 //               P_j is in.
+//   warps 6-7   V converters: each V tile rewritten as fp16 in shared memory once it has
+//               landed (the other operand of P V), off the softmax warps' path.
 //   warps 0-3   softmax, thread = query row: read S_j, running max and sum as fwd_kernel, P_j
-//               (bf16) into the P columns once P V of tile j - 1 is done with them; at the end
+//               (fp16) into the P columns once P V of tile j - 1 is done with them; at the end
 //               O / l through the idle Q tile to global memory by one TMA tensor store.
 // TMEM columns: S [0,128), O [128,192), P [192,256).
 struct FwdSpCfg {
@@ -350,12 +408,15 @@ struct FwdSpCfg {
     static constexpr int Q_BYTES = BM * D * 2;
     static constexpr int KV_BYTES = BN * D * 2;
     static constexpr int SMEM_BYTES = Q_BYTES + 2 * STAGES * KV_BYTES + 1024;
-    static constexpr int THREADS = 192;
-    static constexpr int TMA_WARP = 4, MMA_WARP = 5;
+    static constexpr int THREADS = 256;
+    static constexpr int TMA_WARP = 4, MMA_WARP = 5, CONV_WARP = 6, CONV_THREADS = 64;
+    static constexpr int CONV_PASS = 8;   // 8 loads in flight per thread within 88 registers
+    // two CTAs per SM launch with 128 registers a thread: softmax warpgroup 168, the other 88
+    static constexpr uint32_t REG_SOFTMAX = 168, REG_OTHER = 88;
     static constexpr uint32_t TM_O = 128, TM_P = 192, TM_COLS = 256;
 };
 
-__global__ void __launch_bounds__(192, 2)
+__global__ void __launch_bounds__(256, 2)
     fwd_sp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                   float *__restrict__ lse, int n, int n_qblocks, float scale_log2, int *status)
@@ -370,6 +431,7 @@ __global__ void __launch_bounds__(192, 2)
 
     __shared__ uint64_t bar_q;
     __shared__ uint64_t bar_kf[C::STAGES], bar_ke[C::STAGES], bar_vf[C::STAGES], bar_ve[C::STAGES];
+    __shared__ uint64_t bar_vc[C::STAGES];   // V tile rewritten as fp16
     __shared__ uint64_t bar_s, bar_sread, bar_p, bar_pv, bar_done;
     __shared__ uint32_t tmem_sh;
     __shared__ int abort_sh;
@@ -388,6 +450,7 @@ __global__ void __launch_bounds__(192, 2)
             ptx::mbar_init(&bar_ke[s], 1);
             ptx::mbar_init(&bar_vf[s], 1);
             ptx::mbar_init(&bar_ve[s], 1);
+            ptx::mbar_init(&bar_vc[s], C::CONV_THREADS);
         }
         ptx::mbar_init(&bar_s, 1);
         ptx::mbar_init(&bar_sread, 128);
@@ -405,6 +468,10 @@ __global__ void __launch_bounds__(192, 2)
     ptx::tc_fence_after();
     const uint32_t tmem = tmem_sh;
 
+    // The register split is taken inside each warpgroup's branch, so that the code of each role
+    // is compiled to its own budget.
+    if (warp >= 4) {
+    ptx::setmaxnreg_dec<C::REG_OTHER>();
     if (warp == C::TMA_WARP) {
         // ---------------------------------------------------------------- TMA producer
         if (ptx::elect_one()) {
@@ -426,17 +493,15 @@ __global__ void __launch_bounds__(192, 2)
             // Do not leave the CTA with copies in flight (matters only after a timeout).
             wait_bounded(&bar_q, 0, g);
             for (int j = (nkv > C::STAGES ? nkv - C::STAGES : 0); j < nkv; ++j) {
-                const int s = j % C::STAGES;
-                const uint32_t ph = (j / C::STAGES) & 1;
-                wait_bounded(&bar_kf[s], ph, g);
-                wait_bounded(&bar_vf[s], ph, g);
+                wait_bounded(&bar_kf[j % C::STAGES], (j / C::STAGES) & 1, g);
+                wait_bounded(&bar_vf[j % C::STAGES], (j / C::STAGES) & 1, g);
             }
         }
     } else if (warp == C::MMA_WARP) {
         // ---------------------------------------------------------------- MMA issuer
         if (ptx::elect_one()) {
             const uint32_t idS = ptx::idesc_bf16_f32(128, C::BN, false, false);
-            const uint32_t idO = ptx::idesc_bf16_f32(128, D, false, true);
+            const uint32_t idO = ptx::idesc_f16_f32(128, D, false, true);
             const uint32_t q_base = ptx::smem_u32(sQ), k_base = ptx::smem_u32(sK),
                            v_base = ptx::smem_u32(sV);
             // S = Q K_j^T: both operands K-major (d contiguous).
@@ -447,7 +512,8 @@ __global__ void __launch_bounds__(192, 2)
                                 ptx::sdesc_sw128(k_base + s * C::KV_BYTES + kk * 32, 16, 1024), idS,
                                 kk > 0 ? 1u : 0u);
             };
-            // O += P V_j: P from its TMEM columns (8 columns = 16 keys per step), V MN-major.
+            // O += P V_j: fp16 P from its TMEM columns (8 columns = 16 keys per step), fp16 V
+            // MN-major.
             auto issue_pv = [&](int s, bool acc) {
 #pragma unroll
                 for (int kk = 0; kk < C::BN / 16; ++kk)
@@ -472,7 +538,7 @@ __global__ void __launch_bounds__(192, 2)
                     ptx::mma_commit(&bar_s);
                     ptx::mma_commit(&bar_ke[sn]);
                 }
-                wait_bounded(&bar_vf[s], (j / C::STAGES) & 1, g);
+                wait_bounded(&bar_vc[s], (j / C::STAGES) & 1, g);
                 wait_bounded(&bar_p, j & 1, g);
                 ptx::tc_fence_after();
                 issue_pv(s, j > 0);
@@ -484,6 +550,19 @@ __global__ void __launch_bounds__(192, 2)
             wait_bounded(&bar_done, 0, g);
         }
     } else {
+        // ---------------------------------------------------------------- V to fp16
+        // each V tile rewritten as fp16 in place as soon as it has landed
+        const int ct = (warp - C::CONV_WARP) * 32 + lane;
+        for (int j = 0; j < nkv; ++j) {
+            const int sv = j % C::STAGES;
+            wait_bounded(&bar_vf[sv], (j / C::STAGES) & 1, g);
+            tile_bf16_to_f16<C::KV_BYTES / 16, C::CONV_THREADS, C::CONV_PASS>(ptx::smem_u32(sV + sv * C::KV_BYTES), ct);
+            ptx::fence_proxy_async_smem();
+            ptx::mbar_arrive(&bar_vc[sv]);
+        }
+    }
+    } else {
+        ptx::setmaxnreg_inc<C::REG_SOFTMAX>();
         // ---------------------------------------------------------------- softmax warpgroup
         const int r_local = warp * 32 + lane;   // row of the tile = TMEM lane
         const int row = q0 + r_local;
@@ -527,23 +606,24 @@ __global__ void __launch_bounds__(192, 2)
                 alpha = ptx::ex2(m - m_new);
                 rescale = true;
             }
-            const float neg_m = -m_new;
+            const float neg_m = kPOff - m_new;
             const uint64_t c2 = ptx::f2_pack(scale_log2, scale_log2), nm2 = ptx::f2_pack(neg_m, neg_m);
-            uint64_t acc2[2] = {ptx::f2_pack(0.f, 0.f), ptx::f2_pack(0.f, 0.f)};
-            // P = 2^(x - m) as bf16 pairs, packed into r[0, 64) (each pair lands at or below the
-            // slots it was computed from)
+            uint64_t sum2[2] = {ptx::f2_pack(0.f, 0.f), ptx::f2_pack(0.f, 0.f)};
+            // P = 2^(x - m + kPOff) as fp16 pairs, packed into r[0, 64) (each pair lands at or
+            // below the slots it was computed from)
 #pragma unroll
             for (int i = 0; i < 128; i += 2) {
                 const uint64_t t = ptx::fma_f32x2(ptx::f2_pack(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), c2, nm2);
                 float t0, t1;
                 ptx::f2_unpack(t, t0, t1);
                 const float p0 = ptx::ex2(t0), p1 = ptx::ex2(t1);
-                acc2[(i >> 1) & 1] = ptx::add_f32x2(acc2[(i >> 1) & 1], ptx::f2_pack(p0, p1));
-                r[i >> 1] = ptx::pack_bf16x2(p0, p1);
+                sum2[(i >> 1) & 1] = ptx::add_f32x2(sum2[(i >> 1) & 1], ptx::f2_pack(p0, p1));
+                const uint32_t h = ptx::pack_f16x2(p0, p1);
+                r[i >> 1] = h;
             }
             float sum[4];
-            ptx::f2_unpack(acc2[0], sum[0], sum[1]);
-            ptx::f2_unpack(acc2[1], sum[2], sum[3]);
+            ptx::f2_unpack(sum2[0], sum[0], sum[1]);
+            ptx::f2_unpack(sum2[1], sum[2], sum[3]);
             l = l * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
             m = m_new;
             // P of tile j - 1 has been multiplied into O: its columns and O are ours again
@@ -575,7 +655,7 @@ __global__ void __launch_bounds__(192, 2)
 
         // epilogue: O = O_acc / l (bf16) into the idle Q tile (128-byte swizzle: 16-byte chunk c
         // of row r at chunk c ^ (r % 8)), one TMA tensor store (rows past N clipped);
-        // LSE = (m + log2 l) ln 2
+        // LSE = (m - kPOff + log2 l) ln 2
         wait_bounded(&bar_pv, (nkv - 1) & 1, g);
         ptx::tc_fence_after();
         const float inv_l = 1.f / l;
@@ -602,7 +682,7 @@ __global__ void __launch_bounds__(192, 2)
             ptx::bulk_commit_group();
             ptx::bulk_wait_group<0>();   // complete before the CTA exits
         }
-        if (row < n) lse[(size_t)bh * n + row] = (m + log2f(l)) * kLn2;
+        if (row < n) lse[(size_t)bh * n + row] = (m - kPOff + log2f(l)) * kLn2;
     }
 
     ptx::tc_fence_before();
@@ -622,6 +702,8 @@ __global__ void __launch_bounds__(192, 2)
 //   warp 5      tcgen05: S = Q K_j^T, then O += P V_j; as in fwd_sp_kernel the next S, of this
 //               item or the next, is issued as soon as the softmax warps have read S, and runs
 //               under their exponentials.
+//   warps 6-7   V converters: each V tile rewritten as fp16 in shared memory once it has
+//               landed (the other operand of P V), off the softmax warps' path.
 //   warps 0-3   softmax as fwd_sp_kernel (P in TMEM columns of its own), then the epilogue of
 //               the item: the normalised bf16 tile goes into the item's Q buffer (free once the
 //               item's last S has read it), in the 128-byte-swizzled layout, for the producer
@@ -635,14 +717,19 @@ struct PersistCfg {
     static constexpr int Q_BYTES = BM * D * 2;
     static constexpr int KV_BYTES = BN * D * 2;
     static constexpr int SMEM_BYTES = 2 * Q_BYTES + 2 * STAGES * KV_BYTES + 1024;
-    static constexpr int THREADS = 192;
-    static constexpr int TMA_WARP = 4, MMA_WARP = 5;
+    static constexpr int THREADS = 256;
+    static constexpr int TMA_WARP = 4, MMA_WARP = 5, CONV_WARP = 6, CONV_THREADS = 64;
+    static constexpr int CONV_PASS = 8;   // 8 loads in flight per thread within 88 registers
+    // two CTAs per SM launch with 128 registers a thread; the softmax warpgroup takes 168 of
+    // them, the producer / issuer / converter warpgroup gives back to 88 (128 x 168 + 128 x 88
+    // = 256 x 128)
+    static constexpr uint32_t REG_SOFTMAX = 168, REG_OTHER = 88;
     static constexpr uint32_t TM_O = 128, TM_P = 128 + D;
     static constexpr uint32_t TM_COLS = 128 + D + 64 <= 256 ? 256 : 512;
 };
 
 template <int D>
-__global__ void __launch_bounds__(192, 2)
+__global__ void __launch_bounds__(256, 2)
     fwd_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                           float *__restrict__ lse, int n, int n_qblocks, int n_items,
@@ -657,6 +744,7 @@ __global__ void __launch_bounds__(192, 2)
 
     __shared__ uint64_t bar_qf[2], bar_ost[2];   // Q loaded; O staged in the Q buffer
     __shared__ uint64_t bar_kf[C::STAGES], bar_ke[C::STAGES], bar_vf[C::STAGES], bar_ve[C::STAGES];
+    __shared__ uint64_t bar_vc[C::STAGES];   // V tile rewritten as fp16
     __shared__ uint64_t bar_s, bar_sread, bar_p, bar_pv, bar_done;
     __shared__ uint32_t tmem_sh;
     __shared__ int abort_sh;
@@ -677,6 +765,7 @@ __global__ void __launch_bounds__(192, 2)
             ptx::mbar_init(&bar_ke[s], 1);
             ptx::mbar_init(&bar_vf[s], 1);
             ptx::mbar_init(&bar_ve[s], 1);
+            ptx::mbar_init(&bar_vc[s], C::CONV_THREADS);
         }
         ptx::mbar_init(&bar_s, 1);
         ptx::mbar_init(&bar_sread, 128);
@@ -693,13 +782,15 @@ __global__ void __launch_bounds__(192, 2)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = tmem_sh;
-
+    // The register split is taken inside each warpgroup's branch, so that the code of each role
+    // is compiled to its own budget.
+    if (warp >= 4) {
+    ptx::setmaxnreg_dec<C::REG_OTHER>();
     if (warp == C::TMA_WARP) {
         // ---------------------------------------------------------------- TMA producer
         if (ptx::elect_one()) {
             ptx::tma_prefetch_desc(&tm_q);
             ptx::tma_prefetch_desc(&tm_k);
-            ptx::tma_prefetch_desc(&tm_v);
             // item li - 2's O, staged in Q buffer li % 2, out to global memory
             auto store_o = [&](int li) {
                 const int item = first + li * stride;
@@ -752,7 +843,7 @@ __global__ void __launch_bounds__(192, 2)
         // ---------------------------------------------------------------- MMA issuer
         if (ptx::elect_one()) {
             const uint32_t idS = ptx::idesc_bf16_f32(128, C::BN, false, false);
-            const uint32_t idO = ptx::idesc_bf16_f32(128, D, false, true);
+            const uint32_t idO = ptx::idesc_f16_f32(128, D, false, true);
             const uint32_t q_base = ptx::smem_u32(sQ), k_base = ptx::smem_u32(sK),
                            v_base = ptx::smem_u32(sV);
             auto issue_s = [&](int qb, int s) {
@@ -795,7 +886,7 @@ __global__ void __launch_bounds__(192, 2)
                         else
                             next_s(li + 1, 0, kt + 1);
                     }
-                    wait_bounded(&bar_vf[s], (kt / C::STAGES) & 1, g);
+                    wait_bounded(&bar_vc[s], (kt / C::STAGES) & 1, g);
                     wait_bounded(&bar_p, kt & 1, g);
                     ptx::tc_fence_after();
                     issue_pv(s, j > 0);
@@ -808,6 +899,20 @@ __global__ void __launch_bounds__(192, 2)
             wait_bounded(&bar_done, 0, g);
         }
     } else {
+        // ---------------------------------------------------------------- V to fp16
+        // every V tile of this CTA's ring, in order, rewritten as fp16 in place once it has landed
+        const int ct = (warp - C::CONV_WARP) * 32 + lane;
+        const int n_steps = first < n_items ? ((n_items - first + stride - 1) / stride) * nkv : 0;
+        for (int kv = 0; kv < n_steps; ++kv) {
+            const int sv = kv % C::STAGES;
+            wait_bounded(&bar_vf[sv], (kv / C::STAGES) & 1, g);
+            tile_bf16_to_f16<C::KV_BYTES / 16, C::CONV_THREADS, C::CONV_PASS>(ptx::smem_u32(sV + sv * C::KV_BYTES), ct);
+            ptx::fence_proxy_async_smem();
+            ptx::mbar_arrive(&bar_vc[sv]);
+        }
+    }
+    } else {
+        ptx::setmaxnreg_inc<C::REG_SOFTMAX>();
         // ---------------------------------------------------------------- softmax warpgroup
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
         const uint32_t tS = tmem + lane_off, tO = tmem + lane_off + C::TM_O, tP = tmem + lane_off + C::TM_P;
@@ -854,22 +959,23 @@ __global__ void __launch_bounds__(192, 2)
                     alpha = ptx::ex2(m - m_new);
                     rescale = true;
                 }
-                const float neg_m = -m_new;
+                const float neg_m = kPOff - m_new;
                 const uint64_t c2 = ptx::f2_pack(scale_log2, scale_log2), nm2 = ptx::f2_pack(neg_m, neg_m);
-                uint64_t acc2[2] = {ptx::f2_pack(0.f, 0.f), ptx::f2_pack(0.f, 0.f)};
-                // P = 2^(x - m) as bf16 pairs, packed into r[0, 64)
+                uint64_t sum2[2] = {ptx::f2_pack(0.f, 0.f), ptx::f2_pack(0.f, 0.f)};
+                // P = 2^(x - m + kPOff) as fp16 pairs, packed into r[0, 64)
 #pragma unroll
                 for (int i = 0; i < 128; i += 2) {
                     const uint64_t t = ptx::fma_f32x2(ptx::f2_pack(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), c2, nm2);
                     float t0, t1;
                     ptx::f2_unpack(t, t0, t1);
                     const float p0 = ptx::ex2(t0), p1 = ptx::ex2(t1);
-                    acc2[(i >> 1) & 1] = ptx::add_f32x2(acc2[(i >> 1) & 1], ptx::f2_pack(p0, p1));
-                    r[i >> 1] = ptx::pack_bf16x2(p0, p1);
+                    sum2[(i >> 1) & 1] = ptx::add_f32x2(sum2[(i >> 1) & 1], ptx::f2_pack(p0, p1));
+                    const uint32_t h = ptx::pack_f16x2(p0, p1);
+                    r[i >> 1] = h;
                 }
                 float sum[4];
-                ptx::f2_unpack(acc2[0], sum[0], sum[1]);
-                ptx::f2_unpack(acc2[1], sum[2], sum[3]);
+                ptx::f2_unpack(sum2[0], sum[0], sum[1]);
+                ptx::f2_unpack(sum2[1], sum[2], sum[3]);
                 l = l * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
                 m = m_new;
                 // the previous P V is done with the P columns and O
@@ -901,7 +1007,7 @@ __global__ void __launch_bounds__(192, 2)
 
             // epilogue of this item, once its last P V is done: O / l (bf16) into the Q buffer
             // (128-byte swizzle: 16-byte chunk c of row r at chunk c ^ (r % 8)), then one TMA
-            // store of the tile; LSE = (m + log2 l) ln 2
+            // store of the tile; LSE = (m - kPOff + log2 l) ln 2
             wait_bounded(&bar_pv, (kt - 1) & 1, g);
             ptx::tc_fence_after();
             const float inv_l = 1.f / l;
@@ -928,7 +1034,7 @@ __global__ void __launch_bounds__(192, 2)
             ptx::tc_fence_before();   // O read: the next item's first P V may overwrite it
             ptx::fence_proxy_async_smem();
             ptx::mbar_arrive(&bar_ost[qb]);   // the producer stores the tile
-            if (row < n) lse[(size_t)bh * n + row] = (m + log2f(l)) * kLn2;
+            if (row < n) lse[(size_t)bh * n + row] = (m - kPOff + log2f(l)) * kLn2;
         }
     }
 

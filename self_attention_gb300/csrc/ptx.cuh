@@ -220,6 +220,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
            ((uint32_t)(M >> 4) << 24);
 }
 
+// The same for fp16 A and B (kind::f16 with both operand formats fp16; the two operands of one
+// MMA always share their type).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn_major, bool b_mn_major)
+{
+    return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 // Shared-memory matrix descriptor for the 128-byte swizzled layout (the layout TMA writes
 // with CU_TENSOR_MAP_SWIZZLE_128B: rows of 128 bytes, 8-row atoms of 1024 bytes, the 16-byte
 // chunk c of row r stored at chunk c ^ (r & 7)).  `lbo` / `sbo` are byte strides:
@@ -309,6 +317,20 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 #undef ATTN_R8
 #undef ATTN_W8
 
+// Per-warpgroup register budget (all four warps of a warpgroup execute it together): release
+// registers to the CTA's pool, or wait until the pool can grant more.
+template <uint32_t R>
+__device__ __forceinline__ void setmaxnreg_dec()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
+}
+
+template <uint32_t R>
+__device__ __forceinline__ void setmaxnreg_inc()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
+}
+
 // Named barrier over `nthreads` threads (a multiple of 32), id 1..15 (0 is __syncthreads).
 __device__ __forceinline__ void named_bar(uint32_t id, uint32_t nthreads)
 {
@@ -376,6 +398,40 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+// Two fp32 values -> one register of two fp16 (round to nearest even, gradual underflow,
+// overflow to infinity); `lo` in bits [0,16).
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// A register of two bf16 -> the same two values as fp16 (exact for magnitudes in fp16's normal
+// range [2^-14, 65504]; smaller ones round to fp16's subnormal grid of 2^-24, larger ones become
+// infinite).  bf16 widens to fp32 by a shift, fp32 pairs narrow to fp16 in one conversion.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w)
+{
+    return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// acc + (the fp16 value in the low or the high half of h2), rounded once in fp32.
+__device__ __forceinline__ float add_f16lo(float acc, uint32_t h2)
+{
+    float d;
+    asm("{\n .reg .f16 lo, hi;\n mov.b32 {lo, hi}, %1;\n add.rn.f32.f16 %0, lo, %2;\n}"
+        : "=f"(d) : "r"(h2), "f"(acc));
+    return d;
+}
+
+__device__ __forceinline__ float add_f16hi(float acc, uint32_t h2)
+{
+    float d;
+    asm("{\n .reg .f16 lo, hi;\n mov.b32 {lo, hi}, %1;\n add.rn.f32.f16 %0, hi, %2;\n}"
+        : "=f"(d) : "r"(h2), "f"(acc));
+    return d;
 }
 
 }  // namespace ptx

@@ -4,16 +4,22 @@ The bounds are the ones the project states for this path:
   O    : max |O_gpu - O_ref| <= 1e-2 and ||O_gpu - O_ref||_F / ||O_ref||_F <= 5e-3
   LSE  : max |LSE_gpu - LSE_ref| / max(|LSE_ref|, 1) <= 1e-4
   dQ, dK, dV : relative Frobenius error <= 1e-2
-Two bf16 roundings set a floor under the O error that no kernel with bf16 output and a bf16
-P.V product can beat, and it passes 1e-2 for large |O|:
-  - O itself is bf16: its spacing is 2^-6 on [2, 4) and 2^-5 on [4, 8);
-  - the probabilities enter P.V in bf16, a relative error of at most 2^-9 per weight, so O
-    can move by up to 2^-9 * A_i with A_i = sum_j P_ij |V_j| (the oracle computes A exactly
-    by running on |V|); fp32 accumulation over up to N products adds at most ~2^-10 * A_i
-    more in the worst case.
-The element-wise O bound is therefore max(1e-2, spacing(|O_ref|) + (2^-9 + 2^-10) * A): the
-stated 1e-2 wherever that floor is below it.  check_o reports how many elements needed the
-second branch.
+One rounding sets a floor under the O error that no kernel with bf16 output can beat, and it
+passes 1e-2 for large |O|: O itself is bf16, so even a correctly rounded result is off by up to
+half a spacing, 2^-7 on [2, 4) and 2^-6 on [4, 8).  On top of it the kernel may add:
+  - the weights enter P.V in fp16, each off by a relative 2^-11 at most, while the row sum that
+    divides O adds them unrounded: O moves by sum_j P_ij delta_j V_j, at most 2^-11 * A_i with
+    A_i = sum_j P_ij |V_j| (the oracle computes A exactly by running on |V|);
+  - fp32 accumulation of the products, at most 2^-12 * A_i for the sizes tested;
+  - weights below fp16's normal range (2^-14, against a largest weight of at least 2^7) and V
+    entries below it keep an absolute precision of 2^-25: at most N * 2^-32 * max|V|, under
+    2^-14 for every size tested.
+The element-wise O bound is therefore
+  max(1e-2, spacing(|O_ref|) / 2 + (2^-11 + 2^-12) * A + 2^-14):
+the stated 1e-2 wherever half a bf16 spacing plus the kernel's own error stays below it (|O| < 2
+with A up to about 8, and up to |O| < 4 where A stays near |O|, as it does for the peaked rows
+that make |O| large).  check_o also counts the elements over 1e-2 and reports the smallest |O_ref| among
+them.
 """
 from __future__ import annotations
 
@@ -38,22 +44,35 @@ def rel_fro(got: np.ndarray, ref: np.ndarray) -> float:
 
 def o_bound(ref, a_abs):
     """Element-wise O bound (see the module docstring); a_abs = sum_j P_ij |V_j|."""
-    return np.maximum(O_MAX_ABS, bf16_spacing(ref) + (2.0 ** -9 + 2.0 ** -10) * np.asarray(a_abs))
+    return np.maximum(O_MAX_ABS, 0.5 * bf16_spacing(ref) + (2.0 ** -11 + 2.0 ** -12) * np.asarray(a_abs)
+                      + 2.0 ** -14)
 
 
-def check_o(got, ref, a_abs, where=""):
+# Below this |O| half a bf16 spacing is at most 2^-7, which leaves the kernel's own error room
+# under the stated 1e-2; the workload tests hold every element there to 1e-2 itself.
+O_STRICT_BELOW = 4.0
+
+
+def check_o(got, ref, a_abs, where="", strict=False):
+    """O against the oracle: every element within o_bound, the relative Frobenius error within
+    5e-3, and with `strict` every element with |O_ref| < O_STRICT_BELOW within 1e-2."""
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     err = np.abs(got - ref)
     bound = o_bound(ref, a_abs)
     bad = err > bound
     rf = rel_fro(got, ref)
-    n_ulp = int(((err > O_MAX_ABS) & ~bad).sum())
+    over = err > O_MAX_ABS
     assert not bad.any(), (f"{where} O: {int(bad.sum())} elements over the bound; max abs "
                            f"{err.max():.4g} at |ref|={np.abs(ref.ravel()[err.argmax()]):.4g}")
     assert rf <= O_REL_FRO, f"{where} O: relative Frobenius {rf:.3g} > {O_REL_FRO}"
+    if strict:
+        low = over & (np.abs(ref) < O_STRICT_BELOW)
+        assert not low.any(), (f"{where} O: {int(low.sum())} elements with |O_ref| < {O_STRICT_BELOW} "
+                               f"over {O_MAX_ABS}; largest error there {err[low].max():.4g}")
     return {"o_max_abs": float(err.max()) if err.size else 0.0, "o_rel_fro": rf,
-            "o_elems_over_1e-2_within_rounding_floor": n_ulp,
+            "o_elems_over_1e-2": int(over.sum()),
+            "o_over_1e-2_min_abs_ref": float(np.abs(ref[over]).min()) if over.any() else None,
             "o_ref_max_abs": float(np.abs(ref).max()) if ref.size else 0.0}
 
 

@@ -105,7 +105,7 @@ def test_fwd_other_scale(d):
 @pytest.mark.parametrize("d", [64, 128])
 def test_fwd_extreme_logits(d):
     """Logits with standard deviation 8 (beyond every workload): a few keys carry almost all
-    the weight, where the bf16 rounding of P dominates the error."""
+    the weight, and the weights span far more than fp16's normal range."""
     inp = make_qkv(2, 2, 700, d, seed=13, qk_std=2.0 * math.sqrt(2.0), with_do=False)
     scale = 1.0 / math.sqrt(d)
     o, lse = run_fwd(inp, scale)
@@ -146,7 +146,7 @@ def _sampled_check(w, inp, o, lse, heads, rows_per_head, seed):
         rows = np.unique(np.concatenate([[0, w.N - 1], rng.integers(0, w.N, rows_per_head)]))
         o_ref, lse_ref = oracle.fwd_rows(q[b, h], k[b, h], v[b, h], rows, w.scale)
         a_abs, _ = oracle.fwd_rows(q[b, h], k[b, h], v[b, h].abs(), rows, w.scale)
-        check_o(o[b, h, rows], o_ref, a_abs, f"{w.name} head ({b},{h})")
+        check_o(o[b, h, rows], o_ref, a_abs, f"{w.name} head ({b},{h})", strict=True)
         check_lse(lse[b, h, rows], lse_ref, f"{w.name} head ({b},{h})")
 
 
@@ -163,7 +163,7 @@ def test_fwd_workload_full(name):
         o = o.reshape(w.bh, w.N, w.d)[sel][None]
         lse = lse.reshape(w.bh, w.N)[sel][None]
     o_ref, lse_ref, a_abs = oracle_fwd(inp, w.scale)
-    check_o(o, o_ref, a_abs, name)
+    check_o(o, o_ref, a_abs, name, strict=True)
     check_lse(lse, lse_ref, name)
 
 
