@@ -38,6 +38,13 @@ UNIT = "TFLOPS"
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "bwd_main_long_text.md")
 KERNEL_SOURCES = [os.path.join(ROOT, "self_attention_gb300", "csrc", f)
                   for f in ("attn_bwd.cu", "common.cuh", "ptx.cuh")]
+# the forward kernel's counters, hashed on its own sources
+FWD_PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "fwd_long_text.md")
+FWD_KERNEL_SOURCES = [os.path.join(ROOT, "self_attention_gb300", "csrc", f)
+                      for f in ("attn_fwd.cu", "common.cuh", "ptx.cuh")]
+# NVIDIA's dense bf16 tensor figure for one GB300 GPU (no sparsity), a second denominator
+# beside the measured cuBLAS peak
+DATASHEET_BF16_TFLOPS = 2250.0
 L2_BYTES = 129e6   # GB300 L2 capacity
 # Peaks used when the measured-peaks file is absent (one earlier GB300 measurement).
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -60,6 +67,8 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-configs", action="store_true",
                    help="skip the per-workload forward/backward table")
+    p.add_argument("--no-parity", action="store_true",
+                   help="skip the per-workload forward parity against the oracle")
     return p.parse_args(argv)
 
 
@@ -107,25 +116,25 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources=None) -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in (KERNEL_SOURCES if sources is None else sources):
         with open(f, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(units_per_launch: float):
-    """DRAM bytes per launch of the backward main kernel from the committed ncu summary,
-    scaled from the profiled case by the units (query x key tile pairs) a launch processes;
-    None if the kernel source changed since the counters were taken."""
+def profiled_traffic(units_per_launch: float, summary=None, sources=None):
+    """DRAM bytes per launch of a kernel (by default the backward main kernel) from its
+    committed ncu summary, scaled from the profiled case by the units (query x key tile pairs)
+    a launch processes; None if the kernel's sources changed since the counters were taken."""
     try:
-        text = open(PROFILE_SUMMARY).read()
+        text = open(PROFILE_SUMMARY if summary is None else summary).read()
     except OSError:
         return None
     m_hash = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
     m_bytes = re.search(r"dram_bytes_per_unit:\s*([0-9.eE+]+)", text)
-    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash(sources):
         return None
     return float(m_bytes.group(1)) * units_per_launch
 
@@ -231,6 +240,51 @@ def sample_parity(sa, w, ref: dict, stream) -> dict:
     got = {name: t.double().cpu().numpy() for name, t in
            (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
     return error_norms(got, ref)
+
+
+def parity_by_config(sa, stream, rows_per_head: int = 256) -> dict:
+    """Forward parity on every workload's seeded inputs (the tests' inputs), in the launch
+    configuration the workload runs in: the oracle evaluates sampled rows of three heads (every
+    row where N <= 576) and the GPU's O and LSE there are compared with them.  Reports O max
+    abs error, the elements over the stated 1e-2 with the smallest |O_ref| among them, the
+    largest |O_ref|, O relative Frobenius error and LSE relative error on the sample."""
+    import numpy as np
+    import torch
+    import oracle
+    from self_attention_gb300.inputs import WORKLOADS, make_workload_inputs
+    oracle.build()
+    out = {}
+    for name, w in WORKLOADS.items():
+        inp = make_workload_inputs(w)
+        q, k, v = (inp[x].cuda() for x in ("q", "k", "v"))
+        o, lse = sa.forward(q, k, v, w.scale, stream)
+        torch.cuda.synchronize()
+        o, lse = o.double().cpu().numpy(), lse.double().cpu().numpy()
+        del q, k, v
+        rng = np.random.default_rng(11)
+        err, ref_abs, d2, r2, lse_rel, n = [], [], 0.0, 0.0, 0.0, 0
+        for b, h in ((0, 0), (w.B - 1, w.H - 1), (w.B // 2, w.H // 3)):
+            rows = (np.arange(w.N) if w.N <= 576 else
+                    np.unique(np.concatenate([[0, w.N - 1], rng.integers(0, w.N, rows_per_head)])))
+            o_ref, lse_ref = oracle.fwd_rows(inp["q"][b, h], inp["k"][b, h], inp["v"][b, h], rows, w.scale)
+            o_ref, lse_ref = np.asarray(o_ref, np.float64), np.asarray(lse_ref, np.float64)
+            e = np.abs(o[b, h, rows] - o_ref)
+            err.append(e.ravel())
+            ref_abs.append(np.abs(o_ref).ravel())
+            d2 += float((e ** 2).sum())
+            r2 += float((o_ref ** 2).sum())
+            lse_rel = max(lse_rel, float((np.abs(lse[b, h, rows] - lse_ref) /
+                                          np.maximum(np.abs(lse_ref), 1.0)).max()))
+            n += e.size
+        err, ref_abs = np.concatenate(err), np.concatenate(ref_abs)
+        over = err > 1e-2
+        out[name] = {"elements": n, "o_max_abs": float(err.max()),
+                     "o_ref_at_max": float(ref_abs[err.argmax()]),
+                     "o_elems_over_1e-2": int(over.sum()),
+                     "o_over_1e-2_min_abs_ref": float(ref_abs[over].min()) if over.any() else None,
+                     "o_ref_max_abs": float(ref_abs.max()), "o_rel_fro": math.sqrt(d2 / r2),
+                     "lse_rel": lse_rel}
+    return out
 
 
 def workload_config(w, world: int) -> dict:
@@ -580,10 +634,16 @@ def run_ours(args, world, rank, local):
     per_gpu_bwd = 10.0 * B * H * N * N * D / (local_res["bwd_ms"] * 1e-3) / 1e12
     main_flops = 10.0 * B * H * N * N * D
     achieved = main_flops / (local_res["bwd_main_ms"] * 1e-3) / 1e12
-    peak = peaks["bf16_tflops_sustained"]
-    units = B * H * math.ceil(N / 128) * math.ceil(N / 64)   # (key tile, query tile) pairs
-    # the committed counters are those of the d_k = 128 main kernel; other kernels report none
+    fwd_achieved = 4.0 * B * H * N * N * D / (local_res["fwd_ms"] * 1e-3) / 1e12
+    # The timed region lasts well under a second (steps x ms_per_step), so the kernels run at
+    # burst clocks: the burst peak applies, not the seconds-long sustained one.
+    peak = peaks["bf16_tflops"]
+    units = B * H * math.ceil(N / 128) * math.ceil(N / 64)       # (key tile, query tile) pairs
+    fwd_units = B * H * math.ceil(N / 256) * math.ceil(N / 128)  # (256-query block, key tile)
+    # the committed counters are those of the d_k = 128 kernels; other kernels report none
     traffic = profiled_traffic(units) if D == 128 else None
+    fwd_traffic = (profiled_traffic(fwd_units, FWD_PROFILE_SUMMARY, FWD_KERNEL_SOURCES)
+                   if D == 128 else None)
     if D == 128:
         main_kernel = "bwd_main_kernel<128>"
     elif 128 < N <= 4096:
@@ -598,26 +658,42 @@ def run_ours(args, world, rank, local):
         cpu = {"value": oflops / times[0] / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": desc + f"; wall {times[0]:.2f} s",
                "gpu_errors_on_sample": sample_parity(sa, w, ref, stream)}
+        if not args.no_parity:
+            # the same oracle, on sampled rows of every workload, against the GPU forward
+            cpu["parity_by_config"] = parity_by_config(sa, stream)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": res["step_ms"], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {**workload_config(w, world),
-                   "l2": (f"no flush: inputs (Q,K,V,dO = {in_bytes / 1e6:.0f} MB) are larger than the "
-                          f"{L2_BYTES / 1e6:.0f} MB L2" if l2_flush is None else
-                          f"flushed: inputs (Q,K,V,dO = {in_bytes / 1e6:.0f} MB) fit the "
-                          f"{L2_BYTES / 1e6:.0f} MB L2, so a 256 MB buffer is written before each "
-                          "timed step, outside its events")},
+        "config": workload_config(w, world),
+        "l2": (f"no flush: inputs (Q,K,V,dO = {in_bytes / 1e6:.0f} MB) are larger than the "
+               f"{L2_BYTES / 1e6:.0f} MB L2" if l2_flush is None else
+               f"flushed: inputs (Q,K,V,dO = {in_bytes / 1e6:.0f} MB) fit the "
+               f"{L2_BYTES / 1e6:.0f} MB L2, so a 256 MB buffer is written before each "
+               "timed step, outside its events"),
         "fwd_tflops": per_gpu_fwd, "bwd_tflops": per_gpu_bwd,
         "fwd_pct_of_bf16_peak": 100.0 * per_gpu_fwd / peaks["bf16_tflops"],
         "bwd_pct_of_bf16_peak": 100.0 * per_gpu_bwd / peaks["bf16_tflops"],
-        "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback",
+        "fwd_pct_of_datasheet_bf16": 100.0 * per_gpu_fwd / DATASHEET_BF16_TFLOPS,
+        "peak_source": (f"{peak_src} (MEASURED_PEAKS.json: cuBLAS bf16 GEMM burst {peaks['bf16_tflops']:.0f} "
+                        f"TFLOP/s, copy {peaks['hbm_gbs']:.0f} GB/s)" if peak_src == "measured" else
+                        "fallback (no MEASURED_PEAKS.json)") +
+                       f"; datasheet dense bf16 {DATASHEET_BF16_TFLOPS:.0f} TFLOP/s",
         "roofline": {"kernel": main_kernel,
                      "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "note": f"peak = {peak_src} sustained dense bf16; achieved = 10*B*H*N^2*d "
-                             "flops per launch / CUDA-event launch time"},
+                     "note": f"peak = {peak_src} burst dense bf16 (timed region "
+                             f"{args.steps * res['step_ms'] / 1e3:.2f} s); achieved = 10*B*H*N^2*d "
+                             "flops per launch / CUDA-event launch time; traffic = DRAM bytes per "
+                             "launch from profiles/bwd_main_long_text.md"},
+        "roofline_fwd": {"kernel": "fwd_kernel<128, 2>" if D == 128 else "fwd_persistent_kernel<64>",
+                         "bound": "tensor", "achieved": fwd_achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": fwd_achieved / peak, "traffic": fwd_traffic,
+                         "frac_of_datasheet": fwd_achieved / DATASHEET_BF16_TFLOPS,
+                         "note": "the kernel the >= 60 %-of-peak target is quoted on; achieved = "
+                                 "4*B*H*N^2*d flops per launch / CUDA-event launch time; traffic = "
+                                 "DRAM bytes per launch from profiles/fwd_long_text.md"},
         "cpu_baseline": cpu,
         "qkv_proj": {"workload": "vit_b_mhsa_block X [32, 576, 768] x 3 W [768, 768], 12 heads",
                      **proj},

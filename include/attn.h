@@ -60,6 +60,11 @@ typedef enum {
  *   o       : [B,H,N,d_k] bf16 output, O = softmax(scale * Q K^T) V, rounded to nearest.
  *   lse     : [B,H,N] fp32 output, lse[b,h,i] = log(sum_j exp(scale * q_i . k_j)) (natural
  *             log): the per-row statistic the backward pass recomputes the tiles from.
+ * Arithmetic: scores in fp32 (tensor cores), softmax statistics in fp32, and the product of
+ * the weights with V on fp16 tensor cores: each weight is rounded to fp16 (relative error at
+ * most 2^-11) and V is rounded to fp16, which is exact for |v| in [2^-14, 65504]; smaller
+ * entries keep an absolute precision of 2^-25, and an entry of V above 65504 in magnitude
+ * makes the O rows it contributes to non-finite.  O is normalised by the unrounded row sum.
  */
 attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B,
                      int H, int N, int d_k, float scale, cudaStream_t stream);

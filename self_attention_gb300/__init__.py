@@ -208,11 +208,24 @@ def attn_qkv_proj_bwd(x, w_q, w_k, w_v, dq, dk, dv, dx, dw_q, dw_k, dw_v, B: int
         _ptr(dw_q), _ptr(dw_k), _ptr(dw_v), B, N, D, H, d_k, _stream(stream)), "attn_qkv_proj_bwd")
 
 
+def _device_stream(dev, stream):
+    """The stream to launch on for tensors on `dev`: the device's current stream by default; a
+    torch stream of another device is refused (the kernels would run on one GPU with tensor
+    maps over another's memory)."""
+    if stream is None:
+        return torch.cuda.current_stream(dev)
+    if isinstance(stream, torch.cuda.Stream) and stream.device != dev:
+        raise ValueError(f"stream is on {stream.device}, tensors on {dev}")
+    return stream
+
+
 def qkv_proj(x, w_q, w_k, w_v, H: int, stream=None):
     """Q, K, V = X W_Q, X W_K, X W_V split into H heads: x [B,N,D] bf16 -> 3 x [B,H,N,D/H] bf16."""
     B, N, D = x.shape
-    outs = [torch.empty((B, H, N, D // H), dtype=torch.bfloat16, device=x.device) for _ in range(3)]
-    attn_qkv_proj(x, w_q, w_k, w_v, *outs, B, N, D, H, D // H, stream)
+    with torch.cuda.device(x.device):
+        st = _device_stream(x.device, stream)
+        outs = [torch.empty((B, H, N, D // H), dtype=torch.bfloat16, device=x.device) for _ in range(3)]
+        attn_qkv_proj(x, w_q, w_k, w_v, *outs, B, N, D, H, D // H, st)
     return tuple(outs)
 
 
@@ -220,9 +233,11 @@ def qkv_proj_backward(x, w_q, w_k, w_v, dq, dk, dv, stream=None):
     """Returns (dx [B,N,D] bf16, dw_q, dw_k, dw_v [D,D] fp32)."""
     B, N, D = x.shape
     H = dq.shape[1]
-    dx = torch.empty_like(x)
-    dws = [torch.empty((D, D), dtype=torch.float32, device=x.device) for _ in range(3)]
-    attn_qkv_proj_bwd(x, w_q, w_k, w_v, dq, dk, dv, dx, *dws, B, N, D, H, D // H, stream)
+    with torch.cuda.device(x.device):
+        st = _device_stream(x.device, stream)
+        dx = torch.empty_like(x)
+        dws = [torch.empty((D, D), dtype=torch.float32, device=x.device) for _ in range(3)]
+        attn_qkv_proj_bwd(x, w_q, w_k, w_v, dq, dk, dv, dx, *dws, B, N, D, H, D // H, st)
     return (dx, *dws)
 
 
@@ -253,9 +268,11 @@ def forward(q, k, v, scale: float | None = None, stream=None):
     """Returns (o, lse): o [B,H,N,d_k] bf16, lse [B,H,N] fp32 (natural log)."""
     B, H, N, D = _check_inputs(q, k, v)
     scale = 1.0 / math.sqrt(D) if scale is None else scale
-    o = torch.empty_like(q)
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    attn_fwd(q, k, v, o, lse, B, H, N, D, scale, stream)
+    with torch.cuda.device(q.device):
+        st = _device_stream(q.device, stream)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+        attn_fwd(q, k, v, o, lse, B, H, N, D, scale, st)
     return o, lse
 
 
@@ -264,13 +281,17 @@ def backward(q, k, v, o, dout, lse, scale: float | None = None, stream=None, wor
     """Returns (dq, dk, dv) bf16 for the loss gradient dout = dL/dO.  deterministic=True uses
     attn_bwd_deterministic (no atomics; bitwise reproducible)."""
     B, H, N, D = _check_inputs(q, k, v, o, dout)
+    if lse.device != q.device or (workspace is not None and workspace.device != q.device):
+        raise ValueError("lse and the workspace must be on the tensors' device")
     scale = 1.0 / math.sqrt(D) if scale is None else scale
-    nbytes = attn_bwd_workspace_size(B, H, N, D)
-    if workspace is None:
-        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    fn = attn_bwd_deterministic if deterministic else attn_bwd
-    fn(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace.numel(), B, H, N, D, scale, stream)
+    with torch.cuda.device(q.device):
+        st = _device_stream(q.device, stream)
+        nbytes = attn_bwd_workspace_size(B, H, N, D)
+        if workspace is None:
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        fn = attn_bwd_deterministic if deterministic else attn_bwd
+        fn(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace.numel(), B, H, N, D, scale, st)
     return dq, dk, dv
 
 

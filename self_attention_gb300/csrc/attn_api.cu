@@ -7,6 +7,7 @@
 #include <cudaTypedefs.h>
 #include <cmath>
 #include <cstring>
+#include <atomic>
 #include <cstdio>
 #include <mutex>
 
@@ -14,6 +15,20 @@ namespace attn {
 
 // One status word per device (a __device__ variable lives in every device context).
 __device__ int g_status_word;
+
+int device_sm_count()
+{
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    int sms = cached[dev].load(std::memory_order_relaxed);
+    if (sms == 0) {
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+            sms = 148;
+        cached[dev].store(sms, std::memory_order_relaxed);
+    }
+    return sms;
+}
 
 namespace {
 
@@ -158,7 +173,6 @@ extern "C" attn_status attn_fwd(const void *q, const void *k, const void *v, voi
         (r = make_map(&a.tm_v, v, (int)bh, N, d_k, 128)) != CUDA_SUCCESS ||
         (r = make_map(&a.tm_o, o, (int)bh, N, d_k, 128)) != CUDA_SUCCESS)
         return fail_driver("cuTensorMapEncodeTiled", r);
-    a.v = v;
     a.o = o;
     a.lse = lse;
     a.bh = (int)bh;
@@ -393,6 +407,8 @@ attn_status check_proj(const void *x, const void *const w[3], int B, int N, int 
     if (d_k != 64 && d_k != 128) return ATTN_ERR_UNSUPPORTED_DK;
     if (B < 1 || N < 1 || H < 1 || D != H * d_k || D % 128 != 0) return ATTN_ERR_INVALID_ARG;
     if ((long long)B * N * D >= (1LL << 40) || (long long)B * H > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+    // the token rows B * N index the operand tensor maps as an int
+    if ((long long)B * N > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
     if (!x || !w[0] || !w[1] || !w[2]) return ATTN_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(w[0]) || !aligned16(w[1]) || !aligned16(w[2])) return ATTN_ERR_MISALIGNED;
     return ATTN_OK;

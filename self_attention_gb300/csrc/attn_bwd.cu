@@ -2039,18 +2039,7 @@ __global__ void __launch_bounds__(320, 1)
     }
 }
 
-int g_num_sms = 0;
-
-int elementwise_blocks()
-{
-    if (g_num_sms == 0) {
-        int dev = 0, sms = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        g_num_sms = sms > 0 ? sms : 148;
-    }
-    return 4 * g_num_sms;
-}
+int elementwise_blocks() { return 4 * device_sm_count(); }
 
 template <int D>
 cudaError_t launch_preprocess_d(const BwdArgs &a, bool zero_acc, cudaStream_t stream)
@@ -2099,19 +2088,6 @@ cudaError_t launch_main_wide(const BwdArgs &a, cudaStream_t stream)
     return cudaGetLastError();
 }
 
-int bwd_sm_count()
-{
-    static int cached[64];
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) return 148;
-    if (cached[dev] == 0) {
-        int sms = 0;
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        cached[dev] = sms > 0 ? sms : 148;
-    }
-    return cached[dev];
-}
 
 template <bool WITH_DQ>
 cudaError_t launch_main_persist(const BwdArgs &a, cudaStream_t stream)
@@ -2122,7 +2098,7 @@ cudaError_t launch_main_persist(const BwdArgs &a, cudaStream_t stream)
     if (e != cudaSuccess) return e;
     const int n_kvblocks = (a.n + C::BN - 1) / C::BN;
     const long long items = (long long)n_kvblocks * a.bh;
-    const long long ctas = std::min<long long>(items, bwd_sm_count());
+    const long long ctas = std::min<long long>(items, device_sm_count());
     bwd_main_persist_kernel<WITH_DQ><<<(unsigned)ctas, C::THREADS, C::SMEM_BYTES, stream>>>(
         a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dk, a.tm_dv, a.stats, a.dq_acc, a.n, a.n_pad, n_kvblocks,
         (int)items, a.scale, a.status);

@@ -1046,19 +1046,6 @@ __global__ void __launch_bounds__(256, 2)
     }
 }
 
-int sm_count()
-{
-    static int cached[64];
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) return 148;
-    if (cached[dev] == 0) {
-        int sms = 0;
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        cached[dev] = sms > 0 ? sms : 148;
-    }
-    return cached[dev];
-}
 
 template <int D>
 cudaError_t launch_fwd_persistent(const FwdArgs &a, cudaStream_t stream)
@@ -1070,7 +1057,7 @@ cudaError_t launch_fwd_persistent(const FwdArgs &a, cudaStream_t stream)
     const int n_qblocks = (a.n + C::BM - 1) / C::BM;
     const long long items = (long long)n_qblocks * a.bh;
     // Two CTAs per SM: TMEM (256 columns each), shared memory and registers are sized for it.
-    const long long ctas = std::min<long long>(items, 2LL * sm_count());
+    const long long ctas = std::min<long long>(items, 2LL * device_sm_count());
     fwd_persistent_kernel<D><<<(unsigned)ctas, C::THREADS, C::SMEM_BYTES, stream>>>(
         a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.lse, a.n, n_qblocks,
         (int)items, a.scale * kLog2e, a.status);
@@ -1115,7 +1102,7 @@ cudaError_t launch_fwd(const FwdArgs &a, cudaStream_t stream)
     // are more tiles than resident CTAs (equal to one CTA per tile at long sequences, ahead
     // where items are short), else one CTA per tile
     const long long tiles = (long long)a.bh * ((a.n + 127) / 128);
-    if (tiles > 2LL * sm_count()) return launch_fwd_persistent<64>(a, stream);
+    if (tiles > 2LL * device_sm_count()) return launch_fwd_persistent<64>(a, stream);
     return launch_fwd_sp(a, stream);
 }
 

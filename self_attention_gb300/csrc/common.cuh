@@ -92,16 +92,6 @@ __device__ __forceinline__ void sts_u128(uint32_t addr, uint4 v)
                  : "memory");
 }
 
-// 16 bytes of read-only global memory, not kept in L1.
-__device__ __forceinline__ uint4 ldg_nc_u128(const void *p)
-{
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
 {
     return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));

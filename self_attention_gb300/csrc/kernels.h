@@ -12,7 +12,6 @@ namespace attn {
 struct FwdArgs {
     CUtensorMap tm_q, tm_k, tm_v;   // 3-D maps over [BH, N, d] bf16, 64 x rows boxes, 128-byte swizzle
     CUtensorMap tm_o;               // the same over O (128-row boxes), for tile stores
-    const void *v;                  // [BH, N, d] bf16 (read directly where it is rounded to fp16)
     void *o;                        // [BH, N, d] bf16
     float *lse;                     // [BH, N] fp32
     int bh, n, d;
@@ -34,6 +33,10 @@ struct BwdArgs {
     float scale;
     int *status;
 };
+
+// Streaming multiprocessors of the current device (cached per device, safe to call from several
+// host threads).
+int device_sm_count();
 
 cudaError_t launch_fwd(const FwdArgs &a, cudaStream_t stream);
 // The three stream-ordered phases of the backward pass.

@@ -166,6 +166,10 @@ def test_qkv_proj_argument_errors(lib):
     assert fwd(o=(X, OUT[1], OUT[2])) == 1           # an output over the input
     assert fwd(o=(OUT[0], W[1], OUT[2])) == 1        # an output over a weight
     assert fwd(o=(OUT[0], OUT[0] + 16, OUT[2])) == 1  # two outputs overlapping
+    # B * N token rows past the int range, though B * N * D stays under the 2^40 element bound
+    assert fwd(B=2, N=1 << 30, D=128, H=2) == 1
+    assert lib.attn_qkv_proj_bwd(X, *W, 0x60000000, 0x61000000, 0x62000000, 0x40000000,
+                                 0x50000000, 0x51000000, 0x52000000, 2, 1 << 30, 128, 2, 64, None) == 1
 
     DY = (0x60000000, 0x61000000, 0x62000000)
     DW = (0x50000000, 0x51000000, 0x52000000)        # [256, 256] fp32: 256 KB each
