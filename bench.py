@@ -181,6 +181,19 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu), else the machine type."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return f"{line.split(':', 1)[1].strip()} ({platform.machine()}, {os.cpu_count()} cores)"
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return f"{platform.machine()} ({os.cpu_count()} cores)"
+
+
 def oracle_sample(w, tokens: int):
     """One head (b=0, h=0) of the workload, its first `tokens` tokens (same distribution)."""
     from self_attention_gb300.inputs import make_workload_inputs
@@ -310,7 +323,7 @@ def run_reference(args, world, rank):
         "data": "synthetic",
         "config": workload_config(w, world),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": desc},
+                         "sample": desc, "cpu": cpu_model()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -324,7 +337,9 @@ def time_configs(sa, stream, peaks):
     launch, outside its events; median.  Graph (the small shapes): 20 launches captured in a
     CUDA graph and replayed, mean per launch, without host launch overhead.  GB/s counts the
     algorithmic bytes: forward reads Q, K, V and writes O, LSE; backward reads Q, K, V, O, dO,
-    LSE and writes dQ, dK, dV."""
+    LSE and writes dQ, dK, dV.  fwd_unfused_*: standard attention (attn_fwd_unfused: S and P
+    written to and read back from HBM) on the same inputs, warm, with the fused forward's
+    speedup over it."""
     import torch
     from self_attention_gb300.inputs import WORKLOADS
 
@@ -399,6 +414,25 @@ def time_configs(sa, stream, peaks):
                 row[tag + "_frac_of_hbm_flushed"] = row[tag + "_gbs_flushed"] / peaks["hbm_gbs"]
             row[tag + "_frac_of_hbm"] = row[tag + "_gbs"] / peaks["hbm_gbs"]
             row[tag + "_frac_of_bf16_peak"] = row[tag + "_tflops"] / peaks["bf16_tflops"]
+        # standard attention (S and P through HBM) on the same inputs: the article's comparison
+        ubytes = sa.attn_fwd_unfused_workspace_size(B, H, N, D)
+        uws = torch.empty(ubytes, dtype=torch.uint8, device="cuda")
+        o2, lse2 = torch.empty_like(q), torch.empty_like(lse)
+        unf = lambda: sa.attn_fwd_unfused(q, k, v, o2, lse2, uws, ubytes, B, H, N, D, w.scale, stream)
+        for _ in range(3):
+            unf()
+        a, b = ev(), ev()
+        a.record(stream)
+        for _ in range(rep):
+            unf()
+        b.record(stream)
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) / rep * 1e3
+        row["fwd_unfused_us"] = us
+        row["fwd_unfused_tflops"] = 4 * flops / us / 1e6
+        row["fwd_unfused_workspace_gb"] = ubytes / 1e9
+        row["fwd_fused_speedup"] = us / row["fwd_us"]
+        del uws, o2, lse2
         if sa.attn_get_device_status() != 0:
             raise RuntimeError(f"device status reported a kernel timeout on {name}")
         out[name] = row
@@ -656,7 +690,7 @@ def run_ours(args, world, rank, local):
         ref = {}
         times, oflops, cores, desc = time_oracle(w, args.cpu_baseline_tokens, 1, outputs=ref)
         cpu = {"value": oflops / times[0] / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": desc + f"; wall {times[0]:.2f} s",
+               "sample": desc + f"; wall {times[0]:.2f} s", "cpu": cpu_model(),
                "gpu_errors_on_sample": sample_parity(sa, w, ref, stream)}
         if not args.no_parity:
             # the same oracle, on sampled rows of every workload, against the GPU forward

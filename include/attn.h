@@ -187,6 +187,31 @@ attn_status attn_qkv_proj_bwd(const void *x, const void *w_q, const void *w_k, c
                               int d_k, cudaStream_t stream);
 
 /*
+ * Bytes of device workspace attn_fwd_unfused() needs: the fp32 score matrix S [B,H,N,N] and the
+ * bf16 probabilities P [B,H,N,N], each region 256-byte aligned (6 B H N^2 bytes and padding).
+ * Returns 0 if the sizes are unsupported.
+ */
+size_t attn_fwd_unfused_workspace_size(int B, int H, int N, int d_k);
+
+/*
+ * Standard attention, the comparison point of section 3 ("memory bandwidth bottleneck"): the
+ * same O and LSE as attn_fwd, computed the way the article says frameworks compute it before
+ * FlashAttention: S = scale * Q K^T is written to HBM (fp32, by a batched cuBLAS GEMM), a softmax
+ * pass reads S and writes P = softmax(S) to HBM (bf16, rounded after normalisation) and LSE, and
+ * a second batched cuBLAS GEMM reads P back for O = P V (fp32 accumulation, bf16 output).
+ * Memory grows as N^2 per head; the fused attn_fwd needs none.
+ *   q, k, v, o, lse : as attn_fwd.  workspace : caller-owned device memory of at least
+ *   attn_fwd_unfused_workspace_size() bytes, 256-byte aligned, overwritten.
+ * Errors: as attn_fwd, plus ATTN_ERR_WORKSPACE; B*H*N must fit an int and B*H*N^2 stay below
+ * 2^40 (ATTN_ERR_INVALID_ARG).  cuBLAS is loaded at the first call; if it cannot be loaded or
+ * created the call returns ATTN_ERR_LAUNCH and attn_last_error_string() says why.  Calls are
+ * serialised by a lock (one cuBLAS handle per device).
+ */
+attn_status attn_fwd_unfused(const void *q, const void *k, const void *v, void *o, float *lse,
+                             void *workspace, size_t workspace_bytes, int B, int H, int N, int d_k,
+                             float scale, cudaStream_t stream);
+
+/*
  * Element-wise fp32 addition c[i] = a[i] + b[i], 0 <= i < n: the vector_add_cuda kernel of
  * section 2 ("Practical code comparison: raw CUDA C++ vs OpenAI Triton", the raw CUDA C++
  * version: one element per index, guarded by i < n), used here as the library's HBM bandwidth

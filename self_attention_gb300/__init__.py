@@ -40,7 +40,8 @@ STATUS = {
 EXPORTS = ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess",
            "attn_bwd_main", "attn_bwd_dq_convert", "attn_get_device_status", "attn_status_string",
            "attn_last_error_string", "attn_debug_wait_timeout", "attn_bwd_noalloc", "vector_add",
-           "attn_bwd_deterministic", "attn_qkv_proj", "attn_qkv_proj_bwd")
+           "attn_bwd_deterministic", "attn_qkv_proj", "attn_qkv_proj_bwd",
+           "attn_fwd_unfused", "attn_fwd_unfused_workspace_size")
 
 
 class AttnError(RuntimeError):
@@ -94,6 +95,10 @@ def load_library(path: str = LIB_PATH):
     lib.vector_add.restype = _I
     lib.attn_bwd_noalloc.argtypes = [_VP] * 9 + [_I] * 4 + [_F, _VP]
     lib.attn_bwd_noalloc.restype = _I
+    lib.attn_fwd_unfused_workspace_size.argtypes = [_I] * 4
+    lib.attn_fwd_unfused_workspace_size.restype = _SZ
+    lib.attn_fwd_unfused.argtypes = [_VP] * 6 + [_SZ] + [_I] * 4 + [_F, _VP]
+    lib.attn_fwd_unfused.restype = _I
     lib.attn_debug_wait_timeout.argtypes = [ctypes.c_uint, _VP]
     lib.attn_debug_wait_timeout.restype = _I
     if path == LIB_PATH:
@@ -134,6 +139,18 @@ def attn_fwd(q, k, v, o, lse, B: int, H: int, N: int, d_k: int, scale: float, st
     """Enqueue the forward pass: o and lse written from q, k, v ([B,H,N,d_k] bf16 device)."""
     _raise(load_library().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d_k,
                                    float(scale), _stream(stream)), "attn_fwd")
+
+
+def attn_fwd_unfused_workspace_size(B: int, H: int, N: int, d_k: int) -> int:
+    return int(load_library().attn_fwd_unfused_workspace_size(B, H, N, d_k))
+
+
+def attn_fwd_unfused(q, k, v, o, lse, workspace, workspace_bytes: int, B: int, H: int, N: int,
+                     d_k: int, scale: float, stream=None):
+    """Enqueue standard attention (S and P through HBM): same outputs as attn_fwd."""
+    _raise(load_library().attn_fwd_unfused(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(workspace),
+                                           workspace_bytes, B, H, N, d_k, float(scale), _stream(stream)),
+           "attn_fwd_unfused")
 
 
 def attn_bwd_workspace_size(B: int, H: int, N: int, d_k: int) -> int:
@@ -273,6 +290,21 @@ def forward(q, k, v, scale: float | None = None, stream=None):
         o = torch.empty_like(q)
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
         attn_fwd(q, k, v, o, lse, B, H, N, D, scale, st)
+    return o, lse
+
+
+def forward_unfused(q, k, v, scale: float | None = None, stream=None):
+    """Standard attention (attn_fwd_unfused): returns (o, lse) like forward(), allocating the
+    6 B H N^2 bytes of S and P it materialises."""
+    B, H, N, D = _check_inputs(q, k, v)
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    with torch.cuda.device(q.device):
+        st = _device_stream(q.device, stream)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+        nbytes = attn_fwd_unfused_workspace_size(B, H, N, D)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+        attn_fwd_unfused(q, k, v, o, lse, ws, nbytes, B, H, N, D, scale, st)
     return o, lse
 
 

@@ -19,7 +19,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libattn_gb300.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
 
-SOURCES = ["attn_api.cu", "attn_fwd.cu", "attn_bwd.cu", "vector_add.cu", "proj.cu"]
+SOURCES = ["attn_api.cu", "attn_fwd.cu", "attn_bwd.cu", "vector_add.cu", "proj.cu", "unfused.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               f"-I{INCLUDE}", f"-I{CSRC}"]
@@ -60,7 +60,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         results = list(ex.map(compile_one, SOURCES))
     objs = [o for o, _ in results]
     tmp = LIB_PATH + f".{tag}.tmp"
-    r = subprocess.run([tool, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
+    r = subprocess.run([tool, *ARCH, "-shared", "-o", tmp, *objs, "-ldl"], capture_output=True, text=True)
     for o in objs:
         os.remove(o)
     if r.returncode != 0:

@@ -521,6 +521,84 @@ extern "C" attn_status vector_add(const float *a, const float *b, float *c, long
 }
 
 // --------------------------------------------------------------------------------------------
+// Standard attention (S and P materialised in HBM), the comparison point of the fused path.
+namespace {
+
+struct UnfusedLayout {
+    size_t p_off, total;
+};
+
+UnfusedLayout unfused_layout(long long bh, int N)
+{
+    UnfusedLayout w;
+    w.p_off = align256((size_t)bh * N * N * 4);
+    w.total = w.p_off + align256((size_t)bh * N * N * 2);
+    return w;
+}
+
+attn_status check_unfused(int B, int H, int N, int d_k, float scale)
+{
+    attn_status st = check_sizes(B, H, N, d_k, scale);
+    if (st != ATTN_OK) return st;
+    // one softmax block per row; the library GEMMs take int sizes and long long strides
+    if ((long long)B * H * N > 0x7fffffffLL || (long long)B * H > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+    if ((long long)B * H * N * N >= (1LL << 40)) return ATTN_ERR_INVALID_ARG;
+    return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" size_t attn_fwd_unfused_workspace_size(int B, int H, int N, int d_k)
+{
+    if (check_unfused(B, H, N, d_k, 1.0f) != ATTN_OK) return 0;
+    return unfused_layout((long long)B * H, N).total;
+}
+
+extern "C" attn_status attn_fwd_unfused(const void *q, const void *k, const void *v, void *o, float *lse,
+                                        void *workspace, size_t workspace_bytes, int B, int H, int N,
+                                        int d_k, float scale, cudaStream_t stream)
+{
+    attn_status st = check_unfused(B, H, N, d_k, scale);
+    if (st != ATTN_OK) return st;
+    if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return ATTN_ERR_MISALIGNED;
+    const long long bh = (long long)B * H;
+    const UnfusedLayout lay = unfused_layout(bh, N);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < lay.total)
+        return ATTN_ERR_WORKSPACE;
+    const size_t tbytes = (size_t)bh * N * d_k * 2, lbytes = (size_t)bh * N * 4;
+    const Range ins[3] = {span(q, tbytes), span(k, tbytes), span(v, tbytes)};
+    const Range outs[3] = {span(o, tbytes), span(lse, lbytes), span(workspace, lay.total)};
+    for (int i = 0; i < 3; ++i) {
+        for (const Range &r : ins)
+            if (overlap(r, outs[i])) return ATTN_ERR_INVALID_ARG;
+        for (int j = i + 1; j < 3; ++j)
+            if (overlap(outs[i], outs[j])) return ATTN_ERR_INVALID_ARG;
+    }
+    DeviceState *dev = nullptr;
+    if ((st = device_state(&dev)) != ATTN_OK) return st;
+    FwdArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.o = o;
+    a.lse = lse;
+    a.bh = (int)bh;
+    a.n = N;
+    a.d = d_k;
+    a.scale = scale;
+    a.status = dev->status;
+    float *s = static_cast<float *>(workspace);
+    void *p = static_cast<char *>(workspace) + lay.p_off;
+    cudaError_t e = cudaSuccess;
+    if (const char *why = launch_fwd_unfused(a, q, k, v, s, p, stream, &e)) {
+        if (e != cudaSuccess) return fail(why, e);
+        std::snprintf(t_last_error, sizeof t_last_error, "attn_fwd_unfused: %s", why);
+        return ATTN_ERR_LAUNCH;
+    }
+    return ATTN_OK;
+}
+
+// --------------------------------------------------------------------------------------------
 // The wait self-test kernel: one thread waits on an mbarrier that nothing arrives on.
 namespace attn {
 namespace {

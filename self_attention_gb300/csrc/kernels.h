@@ -61,6 +61,11 @@ cudaError_t launch_proj_fwd(const ProjMaps &m, const ProjArgs &a, cudaStream_t s
 cudaError_t launch_proj_dx(const ProjMaps &m, const ProjArgs &a, cudaStream_t stream);
 cudaError_t launch_proj_dw(const ProjMaps &m, const ProjArgs &a, cudaStream_t stream);
 
+// Standard attention (S and P through HBM; see unfused.cu): returns nullptr on success, else what
+// failed (with *err set where a CUDA call failed).  s: [BH][N][N] fp32, p: [BH][N][N] bf16.
+const char *launch_fwd_unfused(const FwdArgs &a, const void *q, const void *k, const void *v, float *s,
+                               void *p, cudaStream_t stream, cudaError_t *err);
+
 cudaError_t launch_vector_add(const float *a, const float *b, float *c, long long n,
                               cudaStream_t stream);
 cudaError_t launch_wait_selftest(int *status, uint64_t limit_ns, cudaStream_t stream);

@@ -106,6 +106,28 @@ def test_bwd_argument_errors(lib):
     assert lib.attn_bwd_dq_convert(ws, need, 0, 1, 2, 64, 64, ctypes.c_float(0.125), None) == 1
 
 
+def test_unfused_workspace_and_argument_errors(lib):
+    a256 = lambda x: (x + 255) // 256 * 256
+    assert sa.attn_fwd_unfused_workspace_size(1, 2, 100, 64) == a256(2 * 100 * 100 * 4) + a256(2 * 100 * 100 * 2)
+    assert sa.attn_fwd_unfused_workspace_size(1, 2, 100, 96) == 0
+    assert sa.attn_fwd_unfused_workspace_size(1, 1 << 16, 1 << 16, 64) == 0   # B*H*N^2 >= 2^40
+    ws = 0x70000000
+    need = sa.attn_fwd_unfused_workspace_size(1, 2, 64, 64)
+
+    def unf(ws=ws, nbytes=need, d=64, o=O, q=Q, lse=L):
+        return lib.attn_fwd_unfused(q, K, V, o, lse, ws, nbytes, 1, 2, 64, d, ctypes.c_float(0.125), None)
+
+    assert unf(d=80) == 2
+    assert unf(nbytes=need - 1) == 6
+    assert unf(ws=0) == 6
+    assert unf(ws=ws + 16) == 6
+    assert unf(q=0) == 1
+    assert unf(q=Q + 8) == 3
+    assert unf(o=Q) == 1                       # output over an input
+    assert unf(o=ws + 256) == 1                # output inside the workspace
+    assert unf(lse=O + 64) == 1                # lse inside o
+
+
 def test_debug_timeout_argument_range(lib):
     assert lib.attn_debug_wait_timeout(0, None) == 1
     assert lib.attn_debug_wait_timeout(10 ** 7, None) == 1
