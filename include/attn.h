@@ -20,8 +20,8 @@
  *   - `scale` multiplies Q K^T before the softmax; pass 1/sqrt(d_k) for the article's
  *     formula.  It must be finite and > 0.
  *   - Supported: d_k in {64, 128}; B, H, N >= 1; B*H*N*d_k < 2^40 elements; N < 2^31.
- *   - Ownership: the caller allocates and owns every buffer, including the backward
- *     workspace.  The library allocates no device memory on these paths.
+ *   - Ownership: the caller allocates and owns every buffer, including the forward and
+ *     backward workspaces.  The library allocates no device memory on these paths.
  *   - Calls enqueue work on `stream` and return without waiting; only
  *     attn_get_device_status() synchronises (that stream).  Outputs must not overlap inputs.
  *   - The compute calls allocate nothing and never synchronise, so they may be captured in a
@@ -68,6 +68,30 @@ typedef enum {
  */
 attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B,
                      int H, int N, int d_k, float scale, cudaStream_t stream);
+
+/*
+ * Bytes of device workspace attn_fwd_with_workspace() uses for these sizes: an fp16 copy of V
+ * (B*H*N*d_k*2 bytes rounded up to a multiple of 256) where the sequence is long enough for
+ * one rounding pass over V ahead of the forward kernel to cost less than rounding every V tile
+ * in the shared memory of each CTA that reads it (d_k = 64: N >= 2048; d_k = 128: N >= 8192),
+ * else 0.  Also 0 for sizes attn_fwd rejects.
+ */
+size_t attn_fwd_workspace_size(int B, int H, int N, int d_k);
+
+/*
+ * The forward pass of attn_fwd() with a caller workspace (section 3's tiled forward; the
+ * operation, arguments, layouts, arithmetic and results are attn_fwd's, bitwise: V is rounded
+ * to fp16 the same way, only in one pass over HBM into the workspace instead of in shared
+ * memory).  Where attn_fwd_workspace_size() is 0 the call is attn_fwd() and `workspace` may
+ * be null.
+ *   workspace : caller-owned device memory of at least attn_fwd_workspace_size(B,H,N,d_k)
+ *               bytes, 256-byte aligned, overwritten; it must not overlap q, k, v, o or lse.
+ * Errors: as attn_fwd, plus ATTN_ERR_WORKSPACE (null, misaligned or too small where a
+ * workspace is needed) and ATTN_ERR_INVALID_ARG for a workspace overlapping another buffer.
+ */
+attn_status attn_fwd_with_workspace(const void *q, const void *k, const void *v, void *o, float *lse,
+                                    void *workspace, size_t workspace_bytes, int B, int H, int N,
+                                    int d_k, float scale, cudaStream_t stream);
 
 /*
  * Bytes of device workspace attn_bwd() needs for these sizes: two fp32 statistics per row

@@ -23,7 +23,7 @@ import torch
 from .build import LIB_PATH
 
 __all__ = [
-    "AttnError", "attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess",
+    "AttnError", "attn_fwd", "attn_fwd_workspace_size", "attn_fwd_with_workspace", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess",
     "attn_bwd_main", "attn_bwd_dq_convert", "attn_get_device_status",
     "attn_status_string", "attn_last_error_string", "attn_debug_wait_timeout", "attn_bwd_noalloc",
     "vector_add", "attn_bwd_deterministic", "attn_qkv_proj", "attn_qkv_proj_bwd", "qkv_proj",
@@ -37,7 +37,7 @@ STATUS = {
     3: "ATTN_ERR_MISALIGNED", 4: "ATTN_ERR_LAUNCH", 5: "ATTN_ERR_TIMEOUT",
     6: "ATTN_ERR_WORKSPACE", 7: "ATTN_ERR_DEVICE", 8: "ATTN_ERR_TOO_LARGE",
 }
-EXPORTS = ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess",
+EXPORTS = ("attn_fwd", "attn_fwd_workspace_size", "attn_fwd_with_workspace", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess",
            "attn_bwd_main", "attn_bwd_dq_convert", "attn_get_device_status", "attn_status_string",
            "attn_last_error_string", "attn_debug_wait_timeout", "attn_bwd_noalloc", "vector_add",
            "attn_bwd_deterministic", "attn_qkv_proj", "attn_qkv_proj_bwd",
@@ -68,6 +68,10 @@ def load_library(path: str = LIB_PATH):
             "`python -c 'import __graft_entry__ as g; g.build()'` (needs nvcc)")
     lib = ctypes.CDLL(path)
     lib.attn_fwd.argtypes = [_VP] * 5 + [_I] * 4 + [_F, _VP]
+    lib.attn_fwd_workspace_size.argtypes = [_I] * 4
+    lib.attn_fwd_workspace_size.restype = _SZ
+    lib.attn_fwd_with_workspace.argtypes = [_VP] * 6 + [_SZ] + [_I] * 4 + [_F, _VP]
+    lib.attn_fwd_with_workspace.restype = _I
     lib.attn_fwd.restype = _I
     lib.attn_bwd_workspace_size.argtypes = [_I] * 4
     lib.attn_bwd_workspace_size.restype = _SZ
@@ -139,6 +143,19 @@ def attn_fwd(q, k, v, o, lse, B: int, H: int, N: int, d_k: int, scale: float, st
     """Enqueue the forward pass: o and lse written from q, k, v ([B,H,N,d_k] bf16 device)."""
     _raise(load_library().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d_k,
                                    float(scale), _stream(stream)), "attn_fwd")
+
+
+def attn_fwd_workspace_size(B: int, H: int, N: int, d_k: int) -> int:
+    return int(load_library().attn_fwd_workspace_size(B, H, N, d_k))
+
+
+def attn_fwd_with_workspace(q, k, v, o, lse, workspace, workspace_bytes: int, B: int, H: int, N: int,
+                            d_k: int, scale: float, stream=None):
+    """Enqueue attn_fwd with a caller workspace for the fp16 copy of V (None where
+    attn_fwd_workspace_size is 0): the same o and lse, bitwise."""
+    _raise(load_library().attn_fwd_with_workspace(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(workspace) if workspace is not None else None,
+        workspace_bytes, B, H, N, d_k, float(scale), _stream(stream)), "attn_fwd_with_workspace")
 
 
 def attn_fwd_unfused_workspace_size(B: int, H: int, N: int, d_k: int) -> int:
@@ -225,6 +242,17 @@ def attn_qkv_proj_bwd(x, w_q, w_k, w_v, dq, dk, dv, dx, dw_q, dw_k, dw_v, B: int
         _ptr(dw_q), _ptr(dw_k), _ptr(dw_v), B, N, D, H, d_k, _stream(stream)), "attn_qkv_proj_bwd")
 
 
+def _scratch(nbytes: int, dev, st):
+    """Device scratch for a call enqueued on `st`, freed when the caller drops it: torch's
+    caching allocator may hand freed memory to the current stream's next allocation, so a
+    launch stream other than the current one is recorded on the tensor."""
+    t = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    s = st if isinstance(st, torch.cuda.Stream) else torch.cuda.ExternalStream(int(st), device=dev)
+    if s != torch.cuda.current_stream(dev):
+        t.record_stream(s)
+    return t
+
+
 def _device_stream(dev, stream):
     """The stream to launch on for tensors on `dev`: the device's current stream by default; a
     torch stream of another device is refused (the kernels would run on one GPU with tensor
@@ -282,14 +310,17 @@ def _check_inputs(*ts):
 
 
 def forward(q, k, v, scale: float | None = None, stream=None):
-    """Returns (o, lse): o [B,H,N,d_k] bf16, lse [B,H,N] fp32 (natural log)."""
+    """Returns (o, lse): o [B,H,N,d_k] bf16, lse [B,H,N] fp32 (natural log).  Runs
+    attn_fwd_with_workspace, with the fp16 copy of V it wants at long sequences allocated here."""
     B, H, N, D = _check_inputs(q, k, v)
     scale = 1.0 / math.sqrt(D) if scale is None else scale
     with torch.cuda.device(q.device):
         st = _device_stream(q.device, stream)
         o = torch.empty_like(q)
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-        attn_fwd(q, k, v, o, lse, B, H, N, D, scale, st)
+        nbytes = attn_fwd_workspace_size(B, H, N, D)
+        ws = _scratch(nbytes, q.device, st) if nbytes else None
+        attn_fwd_with_workspace(q, k, v, o, lse, ws, nbytes, B, H, N, D, scale, st)
     return o, lse
 
 
@@ -303,7 +334,7 @@ def forward_unfused(q, k, v, scale: float | None = None, stream=None):
         o = torch.empty_like(q)
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
         nbytes = attn_fwd_unfused_workspace_size(B, H, N, D)
-        ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+        ws = _scratch(nbytes, q.device, st)
         attn_fwd_unfused(q, k, v, o, lse, ws, nbytes, B, H, N, D, scale, st)
     return o, lse
 
@@ -320,7 +351,7 @@ def backward(q, k, v, o, dout, lse, scale: float | None = None, stream=None, wor
         st = _device_stream(q.device, stream)
         nbytes = attn_bwd_workspace_size(B, H, N, D)
         if workspace is None:
-            workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+            workspace = _scratch(nbytes, q.device, st)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         fn = attn_bwd_deterministic if deterministic else attn_bwd
         fn(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace.numel(), B, H, N, D, scale, st)

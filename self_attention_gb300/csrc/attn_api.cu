@@ -103,13 +103,14 @@ attn_status device_state(DeviceState **out)
 
 // 3-D map over [BH, N, d] bf16 (innermost first: d, N, BH), boxes of 64 x box_rows x 1 with
 // the 128-byte swizzle.  Rows past N (or past a head) read as zeros.
-CUresult make_map(CUtensorMap *m, const void *base, int bh, int n, int d, int box_rows)
+CUresult make_map(CUtensorMap *m, const void *base, int bh, int n, int d, int box_rows,
+                  CUtensorMapDataType type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16)
 {
     cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)n, (cuuint64_t)bh};
     cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)n * d * 2};
     cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
     cuuint32_t elem[3] = {1, 1, 1};
-    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+    return g_encode(m, type, 3, const_cast<void *>(base), dims, strides,
                     box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -147,8 +148,22 @@ attn_status check_sizes(int B, int H, int N, int d_k, float scale)
 
 using namespace attn;
 
-extern "C" attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
-                                int B, int H, int N, int d_k, float scale, cudaStream_t stream)
+namespace {
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Whether the forward rounds V to fp16 in one pass ahead of the kernel (given a workspace)
+// rather than in each CTA's shared memory.  The in-kernel rewrite costs shared-memory bandwidth
+// per (query block, key tile) pair, the pass HBM traffic per element of V, so the pass pays
+// from a sequence length on, which the per-CTA query rows set (256 at d = 128, 128 at d = 64).
+// Measured crossovers (forward alone, GB300): d = 64 between N = 576 and N = 4096, d = 128
+// between N = 4096 and N = 16384.
+bool fwd_v_prepass(int N, int d_k) { return d_k == 64 ? N >= 2048 : N >= 8192; }
+
+// The forward behind attn_fwd (v16 == nullptr) and attn_fwd_with_workspace (v16: the fp16
+// copy of V, already checked).
+attn_status run_fwd(const void *q, const void *k, const void *v, void *o, float *lse, void *v16,
+                    size_t v16_bytes, int B, int H, int N, int d_k, float scale, cudaStream_t stream)
 {
     attn_status st = check_sizes(B, H, N, d_k, scale);
     if (st != ATTN_OK) return st;
@@ -162,6 +177,13 @@ extern "C" attn_status attn_fwd(const void *q, const void *k, const void *v, voi
     if (overlap(ro, rl)) return ATTN_ERR_INVALID_ARG;
     for (const Range &r : ins)
         if (overlap(r, ro) || overlap(r, rl)) return ATTN_ERR_INVALID_ARG;
+    if (v16) {
+        if ((reinterpret_cast<uintptr_t>(v16) & 255u) || v16_bytes < align256(tbytes)) return ATTN_ERR_WORKSPACE;
+        const Range rw = span(v16, align256(tbytes));
+        if (overlap(rw, ro) || overlap(rw, rl)) return ATTN_ERR_INVALID_ARG;
+        for (const Range &r : ins)
+            if (overlap(r, rw)) return ATTN_ERR_INVALID_ARG;
+    }
 
     DeviceState *dev = nullptr;
     if ((st = device_state(&dev)) != ATTN_OK) return st;
@@ -170,7 +192,8 @@ extern "C" attn_status attn_fwd(const void *q, const void *k, const void *v, voi
     CUresult r;
     if ((r = make_map(&a.tm_q, q, (int)bh, N, d_k, 128)) != CUDA_SUCCESS ||
         (r = make_map(&a.tm_k, k, (int)bh, N, d_k, 128)) != CUDA_SUCCESS ||
-        (r = make_map(&a.tm_v, v, (int)bh, N, d_k, 128)) != CUDA_SUCCESS ||
+        (r = v16 ? make_map(&a.tm_v, v16, (int)bh, N, d_k, 128, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)
+                 : make_map(&a.tm_v, v, (int)bh, N, d_k, 128)) != CUDA_SUCCESS ||
         (r = make_map(&a.tm_o, o, (int)bh, N, d_k, 128)) != CUDA_SUCCESS)
         return fail_driver("cuTensorMapEncodeTiled", r);
     a.o = o;
@@ -179,12 +202,39 @@ extern "C" attn_status attn_fwd(const void *q, const void *k, const void *v, voi
     a.n = N;
     a.d = d_k;
     a.scale = scale;
+    a.v_f16 = v16 ? 1 : 0;
     a.status = dev->status;
-    const cudaError_t e = launch_fwd(a, stream);
+    cudaError_t e;
+    if (v16 && (e = launch_v_to_f16(v, v16, bh * N * d_k, stream)) != cudaSuccess)
+        return fail("attn_fwd_with_workspace V to fp16 launch", e);
+    e = launch_fwd(a, stream);
     return e == cudaSuccess ? ATTN_OK : fail("attn_fwd launch", e);
 }
 
-static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+}  // namespace
+
+extern "C" attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                                int B, int H, int N, int d_k, float scale, cudaStream_t stream)
+{
+    return run_fwd(q, k, v, o, lse, nullptr, 0, B, H, N, d_k, scale, stream);
+}
+
+extern "C" size_t attn_fwd_workspace_size(int B, int H, int N, int d_k)
+{
+    if (check_sizes(B, H, N, d_k, 1.0f) != ATTN_OK || !fwd_v_prepass(N, d_k)) return 0;
+    return align256((size_t)B * H * N * d_k * 2);
+}
+
+extern "C" attn_status attn_fwd_with_workspace(const void *q, const void *k, const void *v, void *o,
+                                               float *lse, void *workspace, size_t workspace_bytes, int B,
+                                               int H, int N, int d_k, float scale, cudaStream_t stream)
+{
+    attn_status st = check_sizes(B, H, N, d_k, scale);
+    if (st != ATTN_OK) return st;
+    if (!fwd_v_prepass(N, d_k)) return run_fwd(q, k, v, o, lse, nullptr, 0, B, H, N, d_k, scale, stream);
+    if (!workspace) return ATTN_ERR_WORKSPACE;
+    return run_fwd(q, k, v, o, lse, workspace, workspace_bytes, B, H, N, d_k, scale, stream);
+}
 
 namespace {
 

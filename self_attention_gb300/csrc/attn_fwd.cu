@@ -16,7 +16,9 @@
 // fwd_sp_kernel where there are fewer tiles than resident CTAs, below):
 //   warp 8      TMA producer: Q tiles once, then a ring of K tiles and a ring of V tiles (128
 //               keys each).
-//   warps 10-11 V converters: each V tile rewritten as fp16 in shared memory once it has landed.
+//   warps 10-11 V converters: each V tile rewritten as fp16 in shared memory once it has landed
+//               (or, where V was rounded to fp16 ahead of the kernel by v_to_f16_kernel, passed
+//               on as it landed: v_f16).
 //   warp 9      tcgen05 issuer: S_t = Q_t K_j^T into TMEM (fp32), then O_t += P_t V_j with
 //               P_t read from TMEM (fp16, written over S_t) and V_j (fp16) from shared memory.
 //   warps 0-7   two softmax warpgroups, one per query tile; thread = one query row.  They
@@ -99,7 +101,7 @@ template <int D, int NQ>
 __global__ void __launch_bounds__(FwdCfg<D, NQ>::THREADS, FwdCfg<D, NQ>::MIN_BLOCKS)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16 *__restrict__ o,
-               float *__restrict__ lse, int n, int n_qblocks, float scale_log2, int *status)
+               float *__restrict__ lse, int n, int n_qblocks, float scale_log2, int v_f16, int *status)
 {
     using C = FwdCfg<D, NQ>;
     extern __shared__ uint8_t smem_raw[];
@@ -256,12 +258,14 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::THREADS, FwdCfg<D, NQ>::MIN_BLO
         }
     } else if (warp >= C::CONV_WARP) {
         // ---------------------------------------------------------------- V to fp16
-        // each V tile rewritten as fp16 in place as soon as it has landed
+        // each V tile rewritten as fp16 in place as soon as it has landed (passed on unchanged
+        // when V is fp16 already)
         const int ct = (warp - C::CONV_WARP) * 32 + lane;
         for (int j = 0; j < nkv; ++j) {
             const int sv = j % C::VSTAGES;
             wait_bounded(&bar_vf[sv], (j / C::VSTAGES) & 1, g);
-            tile_bf16_to_f16<C::KV_BYTES / 16, C::CONV_THREADS, C::CONV_PASS>(ptx::smem_u32(sV + sv * C::KV_BYTES), ct);
+            if (!v_f16)
+                tile_bf16_to_f16<C::KV_BYTES / 16, C::CONV_THREADS, C::CONV_PASS>(ptx::smem_u32(sV + sv * C::KV_BYTES), ct);
             ptx::fence_proxy_async_smem();
             ptx::mbar_arrive(&bar_vc[sv]);
         }
@@ -419,7 +423,7 @@ struct FwdSpCfg {
 __global__ void __launch_bounds__(256, 2)
     fwd_sp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                  float *__restrict__ lse, int n, int n_qblocks, float scale_log2, int *status)
+                  float *__restrict__ lse, int n, int n_qblocks, float scale_log2, int v_f16, int *status)
 {
     using C = FwdSpCfg;
     constexpr int D = C::D;
@@ -551,12 +555,14 @@ __global__ void __launch_bounds__(256, 2)
         }
     } else {
         // ---------------------------------------------------------------- V to fp16
-        // each V tile rewritten as fp16 in place as soon as it has landed
+        // each V tile rewritten as fp16 in place as soon as it has landed (passed on unchanged
+        // when V is fp16 already)
         const int ct = (warp - C::CONV_WARP) * 32 + lane;
         for (int j = 0; j < nkv; ++j) {
             const int sv = j % C::STAGES;
             wait_bounded(&bar_vf[sv], (j / C::STAGES) & 1, g);
-            tile_bf16_to_f16<C::KV_BYTES / 16, C::CONV_THREADS, C::CONV_PASS>(ptx::smem_u32(sV + sv * C::KV_BYTES), ct);
+            if (!v_f16)
+                tile_bf16_to_f16<C::KV_BYTES / 16, C::CONV_THREADS, C::CONV_PASS>(ptx::smem_u32(sV + sv * C::KV_BYTES), ct);
             ptx::fence_proxy_async_smem();
             ptx::mbar_arrive(&bar_vc[sv]);
         }
@@ -733,7 +739,7 @@ __global__ void __launch_bounds__(256, 2)
     fwd_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                           float *__restrict__ lse, int n, int n_qblocks, int n_items,
-                          float scale_log2, int *status)
+                          float scale_log2, int v_f16, int *status)
 {
     using C = PersistCfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -901,12 +907,14 @@ __global__ void __launch_bounds__(256, 2)
     } else {
         // ---------------------------------------------------------------- V to fp16
         // every V tile of this CTA's ring, in order, rewritten as fp16 in place once it has landed
+        // (passed on unchanged when V is fp16 already)
         const int ct = (warp - C::CONV_WARP) * 32 + lane;
         const int n_steps = first < n_items ? ((n_items - first + stride - 1) / stride) * nkv : 0;
         for (int kv = 0; kv < n_steps; ++kv) {
             const int sv = kv % C::STAGES;
             wait_bounded(&bar_vf[sv], (kv / C::STAGES) & 1, g);
-            tile_bf16_to_f16<C::KV_BYTES / 16, C::CONV_THREADS, C::CONV_PASS>(ptx::smem_u32(sV + sv * C::KV_BYTES), ct);
+            if (!v_f16)
+                tile_bf16_to_f16<C::KV_BYTES / 16, C::CONV_THREADS, C::CONV_PASS>(ptx::smem_u32(sV + sv * C::KV_BYTES), ct);
             ptx::fence_proxy_async_smem();
             ptx::mbar_arrive(&bar_vc[sv]);
         }
@@ -1060,7 +1068,7 @@ cudaError_t launch_fwd_persistent(const FwdArgs &a, cudaStream_t stream)
     const long long ctas = std::min<long long>(items, 2LL * device_sm_count());
     fwd_persistent_kernel<D><<<(unsigned)ctas, C::THREADS, C::SMEM_BYTES, stream>>>(
         a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.lse, a.n, n_qblocks,
-        (int)items, a.scale * kLog2e, a.status);
+        (int)items, a.scale * kLog2e, a.v_f16, a.status);
     return cudaGetLastError();
 }
 
@@ -1076,7 +1084,7 @@ cudaError_t launch_fwd_d(const FwdArgs &a, cudaStream_t stream)
     const long long ctas = (long long)n_qblocks * a.bh;
     fwd_kernel<D, NQ><<<(unsigned)ctas, C::THREADS, C::SMEM_BYTES, stream>>>(
         a.tm_q, a.tm_k, a.tm_v, reinterpret_cast<__nv_bfloat16 *>(a.o), a.lse, a.n, n_qblocks,
-        a.scale * kLog2e, a.status);
+        a.scale * kLog2e, a.v_f16, a.status);
     return cudaGetLastError();
 }
 
@@ -1089,11 +1097,45 @@ cudaError_t launch_fwd_sp(const FwdArgs &a, cudaStream_t stream)
     const int n_qblocks = (a.n + C::BM - 1) / C::BM;
     const long long ctas = (long long)n_qblocks * a.bh;
     fwd_sp_kernel<<<(unsigned)ctas, C::THREADS, C::SMEM_BYTES, stream>>>(
-        a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.lse, a.n, n_qblocks, a.scale * kLog2e, a.status);
+        a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.lse, a.n, n_qblocks, a.scale * kLog2e, a.v_f16, a.status);
     return cudaGetLastError();
 }
 
+// V rounded to fp16 once, ahead of the forward kernel, for attn_fwd_with_workspace: the same
+// rounding as tile_bf16_to_f16, over the whole [BH, N, d] tensor at HBM speed, so that the
+// converter warps of every CTA reading V no longer rewrite each tile in shared memory (64
+// CTAs read each V tile at d = 128 and N = 16384).  16-byte vectors, two in flight per
+// thread, grid-stride over whole waves of the SMs; n16 = elements / 8.  V is read once more
+// (by the backward) at most, so its loads stream; the fp16 copy is read right away by the
+// forward kernel and is stored normally.
+__global__ void __launch_bounds__(256)
+    v_to_f16_kernel(const uint4 *__restrict__ v, uint4 *__restrict__ v16, long long n16)
+{
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    auto cvt = [](uint4 x) {
+        return make_uint4(ptx::bf16x2_to_f16x2(x.x), ptx::bf16x2_to_f16x2(x.y), ptx::bf16x2_to_f16x2(x.z),
+                          ptx::bf16x2_to_f16x2(x.w));
+    };
+    for (; i + stride < n16; i += 2 * stride) {
+        const uint4 a = __ldcs(v + i), b = __ldcs(v + i + stride);
+        v16[i] = cvt(a);
+        v16[i + stride] = cvt(b);
+    }
+    if (i < n16) v16[i] = cvt(__ldcs(v + i));
+}
+
 }  // namespace
+
+cudaError_t launch_v_to_f16(const void *v, void *v16, long long elems, cudaStream_t stream)
+{
+    const long long n16 = elems / 8;
+    const long long want = (n16 + 255) / 256;
+    const long long blocks = std::max(1LL, std::min<long long>(want, 8LL * device_sm_count()));
+    v_to_f16_kernel<<<(unsigned)blocks, 256, 0, stream>>>(static_cast<const uint4 *>(v), static_cast<uint4 *>(v16),
+                                                          n16);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_fwd(const FwdArgs &a, cudaStream_t stream)
 {

@@ -16,6 +16,7 @@ struct FwdArgs {
     float *lse;                     // [BH, N] fp32
     int bh, n, d;
     float scale;
+    int v_f16;                      // 1: tm_v maps an fp16 copy of V (no rewrite in shared memory)
     int *status;                    // device status word
 };
 
@@ -39,6 +40,8 @@ struct BwdArgs {
 int device_sm_count();
 
 cudaError_t launch_fwd(const FwdArgs &a, cudaStream_t stream);
+// v16[i] = v[i] rounded from bf16 to fp16, elems a multiple of 8, both 16-byte aligned.
+cudaError_t launch_v_to_f16(const void *v, void *v16, long long elems, cudaStream_t stream);
 // The three stream-ordered phases of the backward pass.
 cudaError_t launch_bwd_preprocess(const BwdArgs &a, cudaStream_t stream);
 cudaError_t launch_bwd_main(const BwdArgs &a, cudaStream_t stream);

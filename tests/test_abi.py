@@ -82,6 +82,33 @@ def test_fwd_argument_errors(lib):
     assert _fwd(lib, B=1 << 20, H=1 << 20) == 1
 
 
+def test_fwd_workspace_size_and_argument_errors(lib):
+    a256 = lambda x: (x + 255) // 256 * 256
+    # an fp16 copy of V from N = 2048 (d_k = 64) and N = 8192 (d_k = 128) on, none below
+    assert sa.attn_fwd_workspace_size(1, 2, 2047, 64) == 0
+    assert sa.attn_fwd_workspace_size(1, 2, 8191, 128) == 0
+    assert sa.attn_fwd_workspace_size(1, 2, 2048, 64) == a256(2 * 2048 * 64 * 2)
+    assert sa.attn_fwd_workspace_size(2, 16, 16384, 128) == 32 * 16384 * 128 * 2
+    assert sa.attn_fwd_workspace_size(1, 2, 4096, 96) == 0
+    assert sa.attn_fwd_workspace_size(0, 2, 4096, 64) == 0
+    need = sa.attn_fwd_workspace_size(1, 2, 2048, 64)
+    ws = 0x70000000
+
+    def fwd(ws=ws, nbytes=need, N=2048, d=64, o=O):
+        return lib.attn_fwd_with_workspace(Q, K, V, o, L, ws, nbytes, 1, 2, N, d, ctypes.c_float(0.125), None)
+
+    assert fwd(d=96) == 2
+    assert fwd(ws=0) == 6
+    assert fwd(nbytes=need - 1) == 6
+    assert fwd(ws=ws + 16) == 6
+    assert fwd(ws=V) == 1                 # the fp16 copy over an input
+    assert fwd(ws=O + 256) == 1           # ... over the output
+    assert fwd(o=Q) == 1
+    # below the threshold the call is attn_fwd: no workspace needed, the same checks
+    assert fwd(ws=0, nbytes=0, N=64, o=Q) == 1
+    assert fwd(ws=0, nbytes=0, N=64, d=128, o=Q + 8) == 3
+
+
 def test_bwd_argument_errors(lib):
     ws = 0x70000000
     need = sa.attn_bwd_workspace_size(1, 2, 64, 64)

@@ -53,6 +53,24 @@ def run_fwd(inp, scale):
     return o.float().cpu().numpy(), lse.cpu().numpy()
 
 
+def run_fwd_ws(inp, scale):
+    """attn_fwd_with_workspace, with canaries around its workspace (the fp16 copy of V) too."""
+    q, k, v = (inp[x].cuda() for x in ("q", "k", "v"))
+    B, H, N, D = q.shape
+    obuf, o = _guarded((B, H, N, D), torch.bfloat16)
+    lbuf, lse = _guarded((B, H, N), torch.float32)
+    nbytes = sa.attn_fwd_workspace_size(B, H, N, D)
+    g = 4096
+    wbuf = torch.full((nbytes + 2 * g,), 0xAB, dtype=torch.uint8, device="cuda")
+    ws = wbuf[g:g + nbytes] if nbytes else None
+    sa.attn_fwd_with_workspace(q, k, v, o, lse, ws, nbytes, B, H, N, D, scale)
+    assert sa.attn_get_device_status() == 0
+    assert _guards_intact(obuf) and _guards_intact(lbuf), "a store escaped the output tensor"
+    assert bool((wbuf[:g] == 0xAB).all()) and bool((wbuf[-g:] == 0xAB).all()), \
+        "a store escaped the workspace"
+    return o.float().cpu().numpy(), lse.cpu().numpy()
+
+
 EDGE_N = [1, 2, 63, 64, 65, 127, 128, 129, 195, 196, 197, 255, 256, 257, 383, 1000, 2049, 2500]
 
 
@@ -114,6 +132,29 @@ def test_fwd_extreme_logits(d):
     check_lse(lse, lse_ref, f"d={d} extreme")
 
 
+@pytest.mark.parametrize("n,d", [(2048, 64), (2049, 64), (2500, 64), (8192, 128), (8200, 128)])
+def test_fwd_workspace_path(n, d):
+    """From the sequence length on where V is rounded to fp16 in one pass ahead of the kernel
+    (attn_fwd_with_workspace), O and LSE are attn_fwd's bitwise (the same fp16 values of V, the
+    same products), and sampled rows match the oracle; ragged N leaves the copy's last tile
+    short, which the tensor map pads with zeros as it does V's."""
+    assert sa.attn_fwd_workspace_size(1, 3, n, d) > 0
+    inp = make_qkv(1, 3, n, d, seed=7700 + n + d, qk_std=2.0, with_do=False)
+    scale = 1.0 / math.sqrt(d)
+    o_ws, lse_ws = run_fwd_ws(inp, scale)
+    o, lse = run_fwd(inp, scale)
+    np.testing.assert_array_equal(o_ws, o)
+    np.testing.assert_array_equal(lse_ws, lse)
+    rng = np.random.default_rng(n)
+    for h in range(3):
+        rows = np.unique(np.concatenate([[0, n - 1], rng.integers(0, n, 40)]))
+        q, k, v = (inp[x][0, h] for x in ("q", "k", "v"))
+        o_ref, lse_ref = oracle.fwd_rows(q, k, v, rows, scale)
+        a_abs, _ = oracle.fwd_rows(q, k, v.abs(), rows, scale)
+        check_o(o_ws[0, h, rows], o_ref, a_abs, f"N={n} d={d} head {h}", strict=True)
+        check_lse(lse_ws[0, h, rows], lse_ref, f"N={n} d={d} head {h}")
+
+
 def test_fwd_deterministic():
     inp = make_qkv(2, 4, 517, 128, seed=5, with_do=False)
     a = run_fwd(inp, 0.088)
@@ -169,10 +210,14 @@ def test_fwd_workload_full(name):
 
 @pytest.mark.parametrize("name", ["vit_l_highres", "long_text"])
 def test_fwd_workload_sampled(name):
-    """Full-size workloads in the benchmark's launch configuration; sampled rows of a few
-    heads against the oracle (each row of the definition is independent)."""
+    """Full-size workloads in the benchmark's launch configuration (attn_fwd_with_workspace);
+    sampled rows of a few heads against the oracle (each row of the definition is
+    independent); attn_fwd gives the same bits."""
     w = WORKLOADS[name]
     inp = make_workload_inputs(w)
-    o, lse = run_fwd(inp, w.scale)
+    o, lse = run_fwd_ws(inp, w.scale)
     heads = [(0, 0), (w.B - 1, w.H - 1), (w.B // 2, w.H // 3)]
     _sampled_check(w, inp, o, lse, heads, rows_per_head=24, seed=1)
+    o2, lse2 = run_fwd(inp, w.scale)   # attn_fwd: V rounded in shared memory, the same bits
+    np.testing.assert_array_equal(o2, o)
+    np.testing.assert_array_equal(lse2, lse)
