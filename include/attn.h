@@ -113,7 +113,10 @@ size_t attn_bwd_workspace_size(int B, int H, int N, int d_k);
  *                      256-byte aligned, owned by the caller; its contents on entry do not
  *                      matter and on return are unspecified.
  * dQ is accumulated across key tiles with fp32 atomic additions, so its low-order bits may
- * differ from run to run; dK and dV are deterministic.
+ * differ from run to run; dK and dV are deterministic.  Exception: for d_k = 64 and N <= 256
+ * over at most one head per SM (and N <= 128 or more heads than half the SMs) one kernel takes
+ * each head whole and accumulates dQ on chip, without atomics: all three gradients are then
+ * bitwise reproducible, and the workspace is not touched.
  */
 attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
                      const void *dout, const float *lse, void *dq, void *dk, void *dv,
@@ -127,7 +130,8 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
  * and errors are those of attn_bwd().  It runs the preprocess, the key-stationary kernel for dK
  * and dV alone, then a query-stationary pass that recomputes S = scale Q K^T and dP = dO V^T
  * tile by tile and accumulates dQ = scale * dS K in order, one CTA per 128 query rows.  It does
- * 14 instead of 10 B*H*N^2*d_k flops.
+ * 14 instead of 10 B*H*N^2*d_k flops.  Where attn_bwd() takes heads whole (d_k = 64, short
+ * sequences, few heads; see there) it runs that same kernel, which needs no atomics.
  */
 attn_status attn_bwd_deterministic(const void *q, const void *k, const void *v, const void *o,
                                    const void *dout, const float *lse, void *dq, void *dk,

@@ -384,6 +384,12 @@ extern "C" attn_status attn_bwd(const void *q, const void *k, const void *v, con
     attn_status st = prepare_bwd(a, kPre | kMain | kConv, q, k, v, o, dout, lse, dq, dk, dv,
                                  workspace, workspace_bytes, B, H, N, d_k, scale);
     if (st != ATTN_OK) return st;
+    // short sequences at d = 64 over few heads: one kernel, dQ accumulated on chip (the
+    // workspace is unused)
+    if (bwd_whole_heads(N, d_k, (long long)B * H)) {
+        const cudaError_t e = launch_bwd_heads(a, stream);
+        return e == cudaSuccess ? ATTN_OK : fail("attn_bwd launch", e);
+    }
     cudaError_t e = launch_bwd_preprocess(a, stream);
     if (e == cudaSuccess) e = launch_bwd_main(a, stream);
     if (e == cudaSuccess) e = launch_bwd_convert(a, stream);
@@ -400,7 +406,9 @@ extern "C" attn_status attn_bwd_deterministic(const void *q, const void *k, cons
     attn_status st = prepare_bwd(a, kPre | kMain | kConv, q, k, v, o, dout, lse, dq, dk, dv,
                                  workspace, workspace_bytes, B, H, N, d_k, scale);
     if (st != ATTN_OK) return st;
-    const cudaError_t e = launch_bwd_deterministic(a, stream);
+    // the whole-head kernel uses no atomics either
+    const cudaError_t e = bwd_whole_heads(N, d_k, (long long)B * H) ? launch_bwd_heads(a, stream)
+                                                                     : launch_bwd_deterministic(a, stream);
     return e == cudaSuccess ? ATTN_OK : fail("attn_bwd_deterministic launch", e);
 }
 

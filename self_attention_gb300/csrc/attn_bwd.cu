@@ -1759,6 +1759,354 @@ __global__ void __launch_bounds__(D128Cfg::THREADS, 1)
     }
 }
 
+// ------------------------------------------------------------------ 2'''. whole heads, d = 64, N <= 256
+// Short sequences at d = 64 (N <= 256: at most two 128-row key blocks and query tiles per
+// head): one CTA takes a whole head (in turn, should there be more heads than CTAs; the
+// dispatch below keeps it to one), so that dQ accumulates in TMEM across the head's key
+// blocks instead of in an fp32 accumulator in L2, and the row statistic D = rowsum(dO o O) is
+// computed on chip.  dQ, dK and dV leave as bf16 straight
+// from TMEM: no preprocess, zero-fill, reduce-add or convert pass, and no atomics (the result
+// is bitwise reproducible).
+//   warp 8      TMA: per head K, V (nkb 128-row key blocks) and Q, dO (nqt 128-row query tiles)
+//               into fixed buffers, once every product of the previous head has read them.
+//   warp 9      tcgen05, per step (key block kb, query tile qt): S^T = K_kb Q_qt^T and
+//               dP^T = V_kb dO_qt^T; once P^T (TMEM) and dS^T (shared memory) are in:
+//               dV_kb += P^T dO_qt, dK_kb += dS^T Q_qt and dQ_qt += dS K_kb; then the next
+//               step's S^T and dP^T (in order after the products that read their columns).
+//   warps 0-7   at each head the per-query statistics (thread = query: -LSE log2 e and -D, D
+//               from O in global memory and dO in shared memory), then per step two
+//               warpgroups on the tile (warpgroup g on queries [64g, 64g + 64), thread = key
+//               row): P^T = 2^(S^T c - LSE2) (bf16 over S^T in TMEM) and dS^T = P^T o (dP^T - D)
+//               (bf16 into shared memory); after each key block's last step dK (warpgroup 0,
+//               times scale) and dV (warpgroup 1), after the head's last step dQ (warpgroup g:
+//               query tile g, times scale), bf16, row by row to global memory.
+// TMEM columns: dQ_0 [0,64), dQ_1 [64,128), dK [128,192), dV [192,256), S^T [256,384),
+// dP^T [384,512).
+struct HeadCfg {
+    static constexpr int D = 64;
+    static constexpr int T = 128;                  // rows of a key block / query tile
+    static constexpr int TILE = T * D * 2;         // one 128-row tile, 16 KB (one 64-column block)
+    static constexpr int STATS_BYTES = 2 * T * 8;  // {-LSE2, -D} of 256 queries, per pair of rows
+    static constexpr int SMEM_BYTES = 10 * TILE + STATS_BYTES + 1024;   // K, V, Q, dO, dS^T: 2 tiles each
+    static constexpr int PDS_WARPS = 8;
+    static constexpr int THREADS = 32 * (PDS_WARPS + 2);
+    static constexpr int TMA_WARP = PDS_WARPS, MMA_WARP = PDS_WARPS + 1;
+    static constexpr uint32_t TM_DQ = 0, TM_DK = 128, TM_DV = 192, TM_S = 256, TM_DP = 384;
+};
+
+__global__ void __launch_bounds__(HeadCfg::THREADS, 1)
+    bwd_head_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const __nv_bfloat16 *__restrict__ o, const float *__restrict__ lse,
+                    __nv_bfloat16 *__restrict__ dq, __nv_bfloat16 *__restrict__ dk,
+                    __nv_bfloat16 *__restrict__ dv, int n, int n_heads, float scale, int *status)
+{
+    using C = HeadCfg;
+    constexpr int D = C::D;
+    constexpr uint32_t PDS_THREADS = 32 * C::PDS_WARPS;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    uint8_t *sK = smem;                       // key blocks 0, 1
+    uint8_t *sV = sK + 2 * C::TILE;
+    uint8_t *sQ = sV + 2 * C::TILE;           // query tiles 0, 1 (two 64-row boxes each)
+    uint8_t *sDO = sQ + 2 * C::TILE;
+    uint8_t *sDS = sDO + 2 * C::TILE;         // dS^T: two 64-query blocks of 128 key rows
+    float *sLD = reinterpret_cast<float *>(sDS + 2 * C::TILE);
+
+    __shared__ uint64_t bar_load, bar_head_done, bar_sdp, bar_ds, bar_kv_ready, bar_kv_read, bar_dq_read;
+    __shared__ uint64_t bar_done;
+    __shared__ uint32_t tmem_sh;
+    __shared__ int abort_sh;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nt = (n + C::T - 1) / C::T;     // key blocks = query tiles (1 or 2)
+    const int first = blockIdx.x, stride = gridDim.x;
+    const Guard g{&abort_sh, status, kWaitLimitNs};
+
+    if (threadIdx.x == 0) {
+        abort_sh = 0;
+        ptx::mbar_init(&bar_load, 1);
+        ptx::mbar_init(&bar_head_done, 1);
+        ptx::mbar_init(&bar_sdp, 1);
+        ptx::mbar_init(&bar_ds, PDS_THREADS);
+        ptx::mbar_init(&bar_kv_ready, 1);
+        ptx::mbar_init(&bar_kv_read, PDS_THREADS);
+        ptx::mbar_init(&bar_dq_read, PDS_THREADS);
+        ptx::mbar_init(&bar_done, 1);
+        ptx::fence_mbar_init();
+    }
+    if (warp == C::MMA_WARP) {
+        ptx::tmem_alloc(&tmem_sh, 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = tmem_sh;
+
+    if (warp == C::TMA_WARP) {
+        // ---------------------------------------------------------------- TMA producer
+        if (ptx::elect_one()) {
+            ptx::tma_prefetch_desc(&tm_q);
+            ptx::tma_prefetch_desc(&tm_k);
+            ptx::tma_prefetch_desc(&tm_v);
+            ptx::tma_prefetch_desc(&tm_do);
+            int hl = 0;
+            for (int bh = first; bh < n_heads; bh += stride, ++hl) {
+                if (hl > 0) wait_bounded(&bar_head_done, (hl - 1) & 1, g);   // the buffers are free
+                ptx::mbar_arrive_expect_tx(&bar_load, 4 * nt * C::TILE);
+                for (int t = 0; t < nt; ++t) {
+                    ptx::tma_load_3d(sK + t * C::TILE, &tm_k, &bar_load, 0, t * C::T, bh);
+                    ptx::tma_load_3d(sV + t * C::TILE, &tm_v, &bar_load, 0, t * C::T, bh);
+                    for (int hh = 0; hh < 2; ++hh) {   // the Q / dO maps have 64-row boxes
+                        ptx::tma_load_3d(sQ + t * C::TILE + hh * 64 * 128, &tm_q, &bar_load, 0,
+                                         t * C::T + hh * 64, bh);
+                        ptx::tma_load_3d(sDO + t * C::TILE + hh * 64 * 128, &tm_do, &bar_load, 0,
+                                         t * C::T + hh * 64, bh);
+                    }
+                }
+            }
+            if (hl > 0) wait_bounded(&bar_load, (hl - 1) & 1, g);   // no copy in flight at exit
+        }
+    } else if (warp == C::MMA_WARP) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (ptx::elect_one()) {
+            const uint32_t idSdP = ptx::idesc_bf16_f32(128, C::T, false, false);
+            const uint32_t idKV = ptx::idesc_bf16_f32(128, D, false, true);
+            const uint32_t idDQ = ptx::idesc_bf16_f32(128, D, true, true);
+            const uint32_t k_base = ptx::smem_u32(sK), v_base = ptx::smem_u32(sV);
+            const uint32_t q_base = ptx::smem_u32(sQ), do_base = ptx::smem_u32(sDO);
+            const uint32_t ds_base = ptx::smem_u32(sDS);
+            // S^T = K_kb Q_qt^T, dP^T = V_kb dO_qt^T: K-major over d (one 64-column block)
+            auto issue_sdp = [&](int kb, int qt) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    ptx::mma_ss(tmem + C::TM_S, ptx::sdesc_sw128(k_base + kb * C::TILE + kk * 32, 16, 1024),
+                                ptx::sdesc_sw128(q_base + qt * C::TILE + kk * 32, 16, 1024), idSdP,
+                                kk > 0 ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    ptx::mma_ss(tmem + C::TM_DP, ptx::sdesc_sw128(v_base + kb * C::TILE + kk * 32, 16, 1024),
+                                ptx::sdesc_sw128(do_base + qt * C::TILE + kk * 32, 16, 1024), idSdP,
+                                kk > 0 ? 1u : 0u);
+            };
+            // K = 128 queries (dV, dK) or 128 keys (dQ), 16 per product
+            auto issue_products = [&](int kb, int qt) {
+                // dV += P^T dO: P^T of queries [16kk, 16kk + 16) in the S^T columns of warpgroup
+                // kk / 4 (64 (kk / 4) + 8 (kk % 4)); dO MN-major (N = d)
+#pragma unroll
+                for (int kk = 0; kk < C::T / 16; ++kk)
+                    ptx::mma_ts(tmem + C::TM_DV, tmem + C::TM_S + (kk >> 2) * 64 + (kk & 3) * 8,
+                                ptx::sdesc_sw128(do_base + qt * C::TILE + kk * 2048, C::TILE, 1024), idKV,
+                                (qt > 0 || kk > 0) ? 1u : 0u);
+                // dK += dS^T Q: dS^T K-major (two 64-query blocks), Q MN-major
+#pragma unroll
+                for (int kk = 0; kk < C::T / 16; ++kk)
+                    ptx::mma_ss(tmem + C::TM_DK,
+                                ptx::sdesc_sw128(ds_base + (kk >> 2) * C::TILE + (kk & 3) * 32, 16, 1024),
+                                ptx::sdesc_sw128(q_base + qt * C::TILE + kk * 2048, C::TILE, 1024), idKV,
+                                (qt > 0 || kk > 0) ? 1u : 0u);
+                // dQ_qt += dS K_kb: A = dS (M = 128 queries) MN-major from the dS^T tile (its two
+                // 64-query blocks TILE bytes apart), B = K_kb MN-major (N = d); K = 128 keys
+#pragma unroll
+                for (int kk = 0; kk < C::T / 16; ++kk)
+                    ptx::mma_ss(tmem + C::TM_DQ + qt * 64, ptx::sdesc_sw128(ds_base + kk * 2048, C::TILE, 1024),
+                                ptx::sdesc_sw128(k_base + kb * C::TILE + kk * 2048, C::TILE, 1024), idDQ,
+                                (kb > 0 || kk > 0) ? 1u : 0u);
+            };
+            int hl = 0, step = 0, kbs = 0;
+            for (int bh = first; bh < n_heads; bh += stride, ++hl) {
+                wait_bounded(&bar_load, hl & 1, g);
+                ptx::tc_fence_after();
+                issue_sdp(0, 0);
+                ptx::mma_commit(&bar_sdp);
+                for (int kb = 0; kb < nt; ++kb) {
+                    for (int qt = 0; qt < nt; ++qt, ++step) {
+                        wait_bounded(&bar_ds, step & 1, g);
+                        // the accumulators restart: dK / dV once the previous key block's
+                        // epilogue has read them, dQ once the previous head's has
+                        if (qt == 0 && kbs > 0) wait_bounded(&bar_kv_read, (kbs - 1) & 1, g);
+                        if (kb == 0 && qt == 0 && hl > 0) wait_bounded(&bar_dq_read, (hl - 1) & 1, g);
+                        ptx::tc_fence_after();
+                        issue_products(kb, qt);
+                        if (qt == nt - 1) ptx::mma_commit(&bar_kv_ready);
+                        const bool last = kb == nt - 1 && qt == nt - 1;
+                        if (!last) {   // over P^T and dP^T, after the products that read them
+                            const int nkb = qt == nt - 1 ? kb + 1 : kb, nqt = qt == nt - 1 ? 0 : qt + 1;
+                            issue_sdp(nkb, nqt);
+                            ptx::mma_commit(&bar_sdp);
+                        }
+                    }
+                    ++kbs;
+                }
+                ptx::mma_commit(&bar_head_done);   // Q, K, V, dO and dS^T read
+            }
+            ptx::mma_commit(&bar_done);
+            wait_bounded(&bar_done, 0, g);
+        }
+    } else {
+        // ---------------------------------------------------------------- P / dS warpgroups
+        const int wg = warp >> 2, cw = warp & 3;
+        const int r = cw * 32 + lane;       // key row of the block = TMEM lane (query row in the dQ epilogue)
+        const uint32_t lane_off = (uint32_t)(cw * 32) << 16;
+        const float scale_log2 = scale * kLog2e;
+        const uint64_t c2 = ptx::f2_pack(scale_log2, scale_log2);
+        const uint32_t tS = tmem + lane_off + C::TM_S + wg * 64, tDP = tmem + lane_off + C::TM_DP + wg * 64;
+        const uint32_t rowp_a = ptx::smem_u32(sDS + wg * C::TILE + r * 128);
+        const uint32_t ld_base = ptx::smem_u32(sLD);
+        int hl = 0, step = 0, kbs = 0;
+        for (int bh = first; bh < n_heads; bh += stride, ++hl) {
+            wait_bounded(&bar_load, hl & 1, g);
+            {   // per-query statistics: thread t takes query t; {-LSE2, -D} interleaved per pair
+                const int qrow = (int)threadIdx.x;   // 0 .. 255
+                float nl = -INFINITY, nd = 0.f;
+                if (qrow < n) {
+                    nl = -lse[(size_t)bh * n + qrow] * kLog2e;
+                    const uint4 *orow = reinterpret_cast<const uint4 *>(o + ((size_t)bh * n + qrow) * D);
+                    const uint32_t dorow = ptx::smem_u32(sDO + (qrow >> 7) * C::TILE + (qrow & 127) * 128);
+                    float acc = 0.f;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint4 ov = __ldg(orow + c);
+                        const uint4 dv4 = lds_u128(dorow + ((c ^ (qrow & 7)) << 4));
+                        const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, dw[4] = {dv4.x, dv4.y, dv4.z, dv4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            acc = fmaf(__uint_as_float(ow[e] << 16), __uint_as_float(dw[e] << 16), acc);
+                            acc = fmaf(__uint_as_float(ow[e] & 0xffff0000u), __uint_as_float(dw[e] & 0xffff0000u), acc);
+                        }
+                    }
+                    nd = -acc;
+                }
+                sts_f32(ld_base + (uint32_t)((qrow >> 1) * 4 + (qrow & 1)) * 4, nl);
+                sts_f32(ld_base + (uint32_t)((qrow >> 1) * 4 + 2 + (qrow & 1)) * 4, nd);
+                ptx::named_bar(1, PDS_THREADS);
+            }
+            for (int kb = 0; kb < nt; ++kb) {
+                const bool key_ok = kb * C::T + r < n;
+                for (int qt = 0; qt < nt; ++qt, ++step) {
+                    // this warpgroup's 64 queries: {-LSE2 pair, -D pair} per two queries
+                    const uint32_t sst_a = ld_base + (uint32_t)(qt * C::T + wg * 64) * 8;
+                    wait_bounded(&bar_sdp, step & 1, g);
+                    ptx::tc_fence_after();
+                    // 16 queries at a time; the next quarter's TMEM loads overlap this quarter's
+                    // math.  P^T of quarter q4 goes to columns [8 q4, 8 q4 + 8) over S^T columns
+                    // already read.
+                    uint32_t sv[2][16], dpv[2][16];
+                    ptx::tmem_ld16(tS, sv[0]);
+                    ptx::tmem_ld16(tDP, dpv[0]);
+                    ptx::tmem_ld_wait();
+                    reg_fence(sv[0]);
+                    reg_fence(dpv[0]);
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const int cur = q4 & 1;
+                        if (q4 < 3) {
+                            ptx::tmem_ld16(tS + (q4 + 1) * 16, sv[cur ^ 1]);
+                            ptx::tmem_ld16(tDP + (q4 + 1) * 16, dpv[cur ^ 1]);
+                        }
+                        uint32_t pp[8], dsp[8];
+                        uint4 st4[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) st4[e] = lds_u128(sst_a + (q4 * 16 + 2 * e) * 8);
+#pragma unroll
+                        for (int c = 0; c < 16; c += 2) {
+                            const uint64_t nl = ((uint64_t)st4[c / 2].y << 32) | st4[c / 2].x;
+                            const uint64_t nd = ((uint64_t)st4[c / 2].w << 32) | st4[c / 2].z;
+                            const uint64_t x = ptx::fma_f32x2(
+                                ptx::f2_pack(__uint_as_float(sv[cur][c]), __uint_as_float(sv[cur][c + 1])), c2, nl);
+                            float x0, x1;
+                            ptx::f2_unpack(x, x0, x1);
+                            float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+                            if (!key_ok) p0 = p1 = 0.f;
+                            const uint64_t pq = ptx::f2_pack(p0, p1);
+                            const uint64_t dsq = ptx::mul_f32x2(
+                                pq, ptx::add_f32x2(ptx::f2_pack(__uint_as_float(dpv[cur][c]), __uint_as_float(dpv[cur][c + 1])), nd));
+                            float ds0, ds1;
+                            ptx::f2_unpack(dsq, ds0, ds1);
+                            pp[c / 2] = ptx::pack_bf16x2(p0, p1);
+                            dsp[c / 2] = ptx::pack_bf16x2(ds0, ds1);
+                        }
+                        ptx::tmem_st8(tS + q4 * 8, pp);
+#pragma unroll
+                        for (int cc = 0; cc < 2; ++cc)
+                            sts_u128(rowp_a + (((q4 * 2 + cc) ^ (r & 7)) << 4),
+                                     make_uint4(dsp[4 * cc], dsp[4 * cc + 1], dsp[4 * cc + 2], dsp[4 * cc + 3]));
+                        if (q4 < 3) {
+                            ptx::tmem_ld_wait();
+                            reg_fence(sv[cur ^ 1]);
+                            reg_fence(dpv[cur ^ 1]);
+                        }
+                    }
+                    ptx::tmem_st_wait();
+                    ptx::fence_proxy_async_smem();
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(&bar_ds);
+                }
+                // the key block's dK (warpgroup 0, times scale) and dV (warpgroup 1), bf16, rows < n
+                wait_bounded(&bar_kv_ready, kbs & 1, g);
+                ptx::tc_fence_after();
+                {
+                    const float mul = wg == 0 ? scale : 1.f;
+                    const uint32_t col0 = wg == 0 ? C::TM_DK : C::TM_DV;
+                    __nv_bfloat16 *dst = (wg == 0 ? dk : dv) + ((size_t)bh * n + kb * C::T + r) * D;
+#pragma unroll
+                    for (int c = 0; c < D; c += 32) {
+                        uint32_t v[32];
+                        ptx::tmem_ld32(tmem + lane_off + col0 + c, v);
+                        ptx::tmem_ld_wait();
+                        reg_fence(v);
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            pk[e] = ptx::pack_bf16x2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+                        if (key_ok) {
+                            uint4 *d4 = reinterpret_cast<uint4 *>(dst + c);
+#pragma unroll
+                            for (int v4 = 0; v4 < 4; ++v4)
+                                d4[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                        }
+                    }
+                }
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(&bar_kv_read);
+                ++kbs;
+            }
+            // the head's dQ: warpgroup g takes query tile g (thread = query row), times scale
+            if (wg < nt) {
+                const int qrow = wg * C::T + r;
+                __nv_bfloat16 *dst = dq + ((size_t)bh * n + qrow) * D;
+#pragma unroll
+                for (int c = 0; c < D; c += 32) {
+                    uint32_t v[32];
+                    ptx::tmem_ld32(tmem + lane_off + C::TM_DQ + wg * 64 + c, v);
+                    ptx::tmem_ld_wait();
+                    reg_fence(v);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        pk[e] = ptx::pack_bf16x2(__uint_as_float(v[2 * e]) * scale, __uint_as_float(v[2 * e + 1]) * scale);
+                    if (qrow < n) {
+                        uint4 *d4 = reinterpret_cast<uint4 *>(dst + c);
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4)
+                            d4[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                    }
+                }
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&bar_dq_read);
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == C::MMA_WARP) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 512);
+    }
+}
+
 // ------------------------------------------------------------------ 4. deterministic dQ pass
 // dQ_i = scale * sum_j dS_ij K_j without atomics: one CTA owns 128 query rows of one head and
 // walks the key tiles (128 keys each) in order, recomputing S = Q K^T and dP = dO V^T on chip.
@@ -2156,6 +2504,31 @@ cudaError_t launch_bwd_deterministic(const BwdArgs &a, cudaStream_t stream)
         e = a.d == 64 ? launch_main_d64<false>(a, stream) : launch_dkdv_d128(a, stream);
     if (e == cudaSuccess) e = a.d == 64 ? launch_dq_d<64>(a, stream) : launch_dq_d<128>(a, stream);
     return e;
+}
+
+// Where it measured faster than the three-kernel path: one head per CTA at most (its heads
+// run one after another, without the other path's overlap of items), and either one key block
+// per head or more heads than half the SMs (with two key blocks the other path runs two CTAs
+// per head, which wins while there are few heads).
+bool bwd_whole_heads(int n, int d, long long bh)
+{
+    if (d != 64 || n > 2 * HeadCfg::T) return false;
+    const int sms = device_sm_count();
+    return bh <= sms && (n <= HeadCfg::T || 2 * bh > sms);
+}
+
+cudaError_t launch_bwd_heads(const BwdArgs &a, cudaStream_t stream)
+{
+    using C = HeadCfg;
+    cudaError_t e = cudaFuncSetAttribute(bwd_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const long long ctas = std::min<long long>(a.bh, device_sm_count());
+    bwd_head_kernel<<<(unsigned)ctas, C::THREADS, C::SMEM_BYTES, stream>>>(
+        a.tm_q, a.tm_k, a.tm_v, a.tm_do, reinterpret_cast<const __nv_bfloat16 *>(a.o), a.lse,
+        reinterpret_cast<__nv_bfloat16 *>(a.dq), reinterpret_cast<__nv_bfloat16 *>(a.dk),
+        reinterpret_cast<__nv_bfloat16 *>(a.dv), a.n, a.bh, a.scale, a.status);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_convert(const BwdArgs &a, cudaStream_t stream)

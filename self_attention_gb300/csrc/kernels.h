@@ -46,6 +46,11 @@ cudaError_t launch_v_to_f16(const void *v, void *v16, long long elems, cudaStrea
 cudaError_t launch_bwd_preprocess(const BwdArgs &a, cudaStream_t stream);
 cudaError_t launch_bwd_main(const BwdArgs &a, cudaStream_t stream);
 cudaError_t launch_bwd_convert(const BwdArgs &a, cudaStream_t stream);
+// Short sequences at d = 64 (N <= 256): the whole backward (statistics, dQ, dK, dV) in one
+// kernel, one CTA per head, dQ accumulated on chip; used by attn_bwd and
+// attn_bwd_deterministic where bwd_whole_heads(n, d, B*H) holds.
+bool bwd_whole_heads(int n, int d, long long bh);
+cudaError_t launch_bwd_heads(const BwdArgs &a, cudaStream_t stream);
 // The deterministic backward: preprocess (no accumulator), the main kernel without its dQ part,
 // then a query-stationary pass that computes dQ without atomics.
 cudaError_t launch_bwd_deterministic(const BwdArgs &a, cudaStream_t stream);
