@@ -261,7 +261,9 @@ def parity_by_config(sa, stream, rows_per_head: int = 256) -> dict:
     configuration the workload runs in: the oracle evaluates sampled rows of three heads (every
     row where N <= 576) and the GPU's O and LSE there are compared with them.  Reports O max
     abs error, the elements over the stated 1e-2 with the smallest |O_ref| among them, the
-    largest |O_ref|, O relative Frobenius error and LSE relative error on the sample."""
+    largest |O_ref|, O relative Frobenius error and LSE relative error on the sample; and the
+    error of O before its bf16 rounding (attn_fwd_diagnostic, the same arithmetic), which
+    separates the kernel's own error from the output rounding."""
     import numpy as np
     import torch
     import oracle
@@ -272,17 +274,20 @@ def parity_by_config(sa, stream, rows_per_head: int = 256) -> dict:
         inp = make_workload_inputs(w)
         q, k, v = (inp[x].cuda() for x in ("q", "k", "v"))
         o, lse = sa.forward(q, k, v, w.scale, stream)
+        _, _, o32 = sa.forward_diagnostic(q, k, v, w.scale, stream)
         torch.cuda.synchronize()
         o, lse = o.double().cpu().numpy(), lse.double().cpu().numpy()
+        o32 = o32.double().cpu().numpy()
         del q, k, v
         rng = np.random.default_rng(11)
-        err, ref_abs, d2, r2, lse_rel, n = [], [], 0.0, 0.0, 0.0, 0
+        err, ref_abs, d2, r2, lse_rel, n, err32 = [], [], 0.0, 0.0, 0.0, 0, 0.0
         for b, h in ((0, 0), (w.B - 1, w.H - 1), (w.B // 2, w.H // 3)):
             rows = (np.arange(w.N) if w.N <= 576 else
                     np.unique(np.concatenate([[0, w.N - 1], rng.integers(0, w.N, rows_per_head)])))
             o_ref, lse_ref = oracle.fwd_rows(inp["q"][b, h], inp["k"][b, h], inp["v"][b, h], rows, w.scale)
             o_ref, lse_ref = np.asarray(o_ref, np.float64), np.asarray(lse_ref, np.float64)
             e = np.abs(o[b, h, rows] - o_ref)
+            err32 = max(err32, float(np.abs(o32[b, h, rows] - o_ref).max()))
             err.append(e.ravel())
             ref_abs.append(np.abs(o_ref).ravel())
             d2 += float((e ** 2).sum())
@@ -297,7 +302,7 @@ def parity_by_config(sa, stream, rows_per_head: int = 256) -> dict:
                      "o_elems_over_1e-2": int(over.sum()),
                      "o_over_1e-2_min_abs_ref": float(ref_abs[over].min()) if over.any() else None,
                      "o_ref_max_abs": float(ref_abs.max()), "o_rel_fro": math.sqrt(d2 / r2),
-                     "lse_rel": lse_rel}
+                     "o_fp32_max_abs": err32, "lse_rel": lse_rel}
     return out
 
 

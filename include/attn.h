@@ -70,6 +70,19 @@ attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float
                      int H, int N, int d_k, float scale, cudaStream_t stream);
 
 /*
+ * Diagnostic forward: attn_fwd() (same o and lse, bitwise) that also writes O before it is
+ * rounded to bf16, so that the arithmetic's own error can be told apart from the output
+ * rounding (section 1's Attention(Q,K,V); the bf16 o is exactly o32 rounded to nearest).
+ *   o32 : [B,H,N,d_k] fp32 device output, 16-byte aligned, written with per-row stores (slow:
+ *         for tests and measurements, not for training).
+ * Errors: as attn_fwd; ATTN_ERR_INVALID_ARG for a null o32 or one overlapping another buffer,
+ * ATTN_ERR_MISALIGNED for a misaligned one.
+ */
+attn_status attn_fwd_diagnostic(const void *q, const void *k, const void *v, void *o, float *lse,
+                                float *o32, int B, int H, int N, int d_k, float scale,
+                                cudaStream_t stream);
+
+/*
  * Bytes of device workspace attn_fwd_with_workspace() uses for these sizes: an fp16 copy of V
  * (B*H*N*d_k*2 bytes rounded up to a multiple of 256) where the sequence is long enough for
  * one rounding pass over V ahead of the forward kernel to cost less than rounding every V tile

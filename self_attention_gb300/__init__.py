@@ -23,12 +23,13 @@ import torch
 from .build import LIB_PATH
 
 __all__ = [
-    "AttnError", "attn_fwd", "attn_fwd_workspace_size", "attn_fwd_with_workspace", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess",
+    "AttnError", "attn_fwd", "attn_fwd_workspace_size", "attn_fwd_with_workspace", "attn_fwd_diagnostic",
+    "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess",
     "attn_bwd_main", "attn_bwd_dq_convert", "attn_get_device_status",
     "attn_status_string", "attn_last_error_string", "attn_debug_wait_timeout", "attn_bwd_noalloc",
     "vector_add", "attn_bwd_deterministic", "attn_qkv_proj", "attn_qkv_proj_bwd", "qkv_proj",
     "qkv_proj_backward",
-    "forward", "backward", "attention",
+    "forward", "forward_diagnostic", "backward", "attention",
     "load_library", "STATUS",
 ]
 
@@ -37,7 +38,7 @@ STATUS = {
     3: "ATTN_ERR_MISALIGNED", 4: "ATTN_ERR_LAUNCH", 5: "ATTN_ERR_TIMEOUT",
     6: "ATTN_ERR_WORKSPACE", 7: "ATTN_ERR_DEVICE", 8: "ATTN_ERR_TOO_LARGE",
 }
-EXPORTS = ("attn_fwd", "attn_fwd_workspace_size", "attn_fwd_with_workspace", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess",
+EXPORTS = ("attn_fwd", "attn_fwd_workspace_size", "attn_fwd_with_workspace", "attn_fwd_diagnostic", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess",
            "attn_bwd_main", "attn_bwd_dq_convert", "attn_get_device_status", "attn_status_string",
            "attn_last_error_string", "attn_debug_wait_timeout", "attn_bwd_noalloc", "vector_add",
            "attn_bwd_deterministic", "attn_qkv_proj", "attn_qkv_proj_bwd",
@@ -72,6 +73,8 @@ def load_library(path: str = LIB_PATH):
     lib.attn_fwd_workspace_size.restype = _SZ
     lib.attn_fwd_with_workspace.argtypes = [_VP] * 6 + [_SZ] + [_I] * 4 + [_F, _VP]
     lib.attn_fwd_with_workspace.restype = _I
+    lib.attn_fwd_diagnostic.argtypes = [_VP] * 6 + [_I] * 4 + [_F, _VP]
+    lib.attn_fwd_diagnostic.restype = _I
     lib.attn_fwd.restype = _I
     lib.attn_bwd_workspace_size.argtypes = [_I] * 4
     lib.attn_bwd_workspace_size.restype = _SZ
@@ -156,6 +159,13 @@ def attn_fwd_with_workspace(q, k, v, o, lse, workspace, workspace_bytes: int, B:
     _raise(load_library().attn_fwd_with_workspace(
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(workspace) if workspace is not None else None,
         workspace_bytes, B, H, N, d_k, float(scale), _stream(stream)), "attn_fwd_with_workspace")
+
+
+def attn_fwd_diagnostic(q, k, v, o, lse, o32, B: int, H: int, N: int, d_k: int, scale: float, stream=None):
+    """Enqueue attn_fwd that also writes O before its bf16 rounding into o32 ([B,H,N,d_k] fp32)."""
+    _raise(load_library().attn_fwd_diagnostic(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(o32),
+                                              B, H, N, d_k, float(scale), _stream(stream)),
+           "attn_fwd_diagnostic")
 
 
 def attn_fwd_unfused_workspace_size(B: int, H: int, N: int, d_k: int) -> int:
@@ -322,6 +332,20 @@ def forward(q, k, v, scale: float | None = None, stream=None):
         ws = _scratch(nbytes, q.device, st) if nbytes else None
         attn_fwd_with_workspace(q, k, v, o, lse, ws, nbytes, B, H, N, D, scale, st)
     return o, lse
+
+
+def forward_diagnostic(q, k, v, scale: float | None = None, stream=None):
+    """(o, lse, o32): forward()'s results and O before its bf16 rounding (fp32), for measuring
+    the kernel's own error apart from the output rounding."""
+    B, H, N, D = _check_inputs(q, k, v)
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    with torch.cuda.device(q.device):
+        st = _device_stream(q.device, stream)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+        o32 = torch.empty((B, H, N, D), dtype=torch.float32, device=q.device)
+        attn_fwd_diagnostic(q, k, v, o, lse, o32, B, H, N, D, scale, st)
+    return o, lse, o32
 
 
 def forward_unfused(q, k, v, scale: float | None = None, stream=None):

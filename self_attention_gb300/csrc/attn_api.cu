@@ -160,10 +160,11 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 // between N = 4096 and N = 16384.
 bool fwd_v_prepass(int N, int d_k) { return d_k == 64 ? N >= 2048 : N >= 8192; }
 
-// The forward behind attn_fwd (v16 == nullptr) and attn_fwd_with_workspace (v16: the fp16
-// copy of V, already checked).
+// The forward behind attn_fwd (v16 == nullptr), attn_fwd_with_workspace (v16: the fp16 copy of
+// V) and attn_fwd_diagnostic (o32: O before its bf16 rounding as well).
 attn_status run_fwd(const void *q, const void *k, const void *v, void *o, float *lse, void *v16,
-                    size_t v16_bytes, int B, int H, int N, int d_k, float scale, cudaStream_t stream)
+                    size_t v16_bytes, int B, int H, int N, int d_k, float scale, cudaStream_t stream,
+                    float *o32 = nullptr)
 {
     attn_status st = check_sizes(B, H, N, d_k, scale);
     if (st != ATTN_OK) return st;
@@ -184,6 +185,13 @@ attn_status run_fwd(const void *q, const void *k, const void *v, void *o, float 
         for (const Range &r : ins)
             if (overlap(r, rw)) return ATTN_ERR_INVALID_ARG;
     }
+    if (o32) {
+        if (!aligned16(o32)) return ATTN_ERR_MISALIGNED;
+        const Range r32 = span(o32, tbytes * 2);
+        if (overlap(r32, ro) || overlap(r32, rl)) return ATTN_ERR_INVALID_ARG;
+        for (const Range &r : ins)
+            if (overlap(r, r32)) return ATTN_ERR_INVALID_ARG;
+    }
 
     DeviceState *dev = nullptr;
     if ((st = device_state(&dev)) != ATTN_OK) return st;
@@ -203,6 +211,7 @@ attn_status run_fwd(const void *q, const void *k, const void *v, void *o, float 
     a.d = d_k;
     a.scale = scale;
     a.v_f16 = v16 ? 1 : 0;
+    a.o32 = o32;
     a.status = dev->status;
     cudaError_t e;
     if (v16 && (e = launch_v_to_f16(v, v16, bh * N * d_k, stream)) != cudaSuccess)
@@ -217,6 +226,14 @@ extern "C" attn_status attn_fwd(const void *q, const void *k, const void *v, voi
                                 int B, int H, int N, int d_k, float scale, cudaStream_t stream)
 {
     return run_fwd(q, k, v, o, lse, nullptr, 0, B, H, N, d_k, scale, stream);
+}
+
+extern "C" attn_status attn_fwd_diagnostic(const void *q, const void *k, const void *v, void *o, float *lse,
+                                           float *o32, int B, int H, int N, int d_k, float scale,
+                                           cudaStream_t stream)
+{
+    if (!o32) return ATTN_ERR_INVALID_ARG;
+    return run_fwd(q, k, v, o, lse, nullptr, 0, B, H, N, d_k, scale, stream, o32);
 }
 
 extern "C" size_t attn_fwd_workspace_size(int B, int H, int N, int d_k)

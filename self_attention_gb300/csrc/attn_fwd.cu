@@ -74,6 +74,17 @@ __device__ __forceinline__ void tile_bf16_to_f16(uint32_t base, int ct)
     }
 }
 
+// Diagnostic output: 32 consecutive columns of a row of O before its bf16 rounding (acc / l
+// in fp32), as attn_fwd_diagnostic returns them.
+__device__ __forceinline__ void store_o32(float *dst, const uint32_t (&ov)[32], float inv_l)
+{
+    float4 *d4 = reinterpret_cast<float4 *>(dst);
+#pragma unroll
+    for (int v4 = 0; v4 < 8; ++v4)
+        d4[v4] = make_float4(__uint_as_float(ov[4 * v4]) * inv_l, __uint_as_float(ov[4 * v4 + 1]) * inv_l,
+                             __uint_as_float(ov[4 * v4 + 2]) * inv_l, __uint_as_float(ov[4 * v4 + 3]) * inv_l);
+}
+
 template <int D, int NQ_>
 struct FwdCfg {
     static constexpr int BM = 128;  // query rows per tile (= TMEM lanes)
@@ -101,7 +112,8 @@ template <int D, int NQ>
 __global__ void __launch_bounds__(FwdCfg<D, NQ>::THREADS, FwdCfg<D, NQ>::MIN_BLOCKS)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16 *__restrict__ o,
-               float *__restrict__ lse, int n, int n_qblocks, float scale_log2, int v_f16, int *status)
+               float *__restrict__ lse, float *__restrict__ o32, int n, int n_qblocks, float scale_log2,
+               int v_f16, int *status)
 {
     using C = FwdCfg<D, NQ>;
     extern __shared__ uint8_t smem_raw[];
@@ -374,6 +386,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::THREADS, FwdCfg<D, NQ>::MIN_BLO
             for (int i = 0; i < 16; ++i)
                 pk[i] = ptx::pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l,
                                          __uint_as_float(ov[2 * i + 1]) * inv_l);
+            if (o32 && row < n) store_o32(o32 + ((size_t)bh * n + row) * D + c, ov, inv_l);
             if (row < n) {
                 uint4 *dst = reinterpret_cast<uint4 *>(orow + c);
 #pragma unroll
@@ -423,7 +436,8 @@ struct FwdSpCfg {
 __global__ void __launch_bounds__(256, 2)
     fwd_sp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                  float *__restrict__ lse, int n, int n_qblocks, float scale_log2, int v_f16, int *status)
+                  float *__restrict__ lse, float *__restrict__ o32, int n, int n_qblocks, float scale_log2,
+                  int v_f16, int *status)
 {
     using C = FwdSpCfg;
     constexpr int D = C::D;
@@ -676,6 +690,7 @@ __global__ void __launch_bounds__(256, 2)
 #pragma unroll
             for (int i = 0; i < 16; ++i)
                 pk[i] = ptx::pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l);
+            if (o32 && row < n) store_o32(o32 + ((size_t)bh * n + row) * D + c, ov, inv_l);
 #pragma unroll
             for (int v4 = 0; v4 < 4; ++v4)
                 sts_u128(srow + ((((c >> 3) + v4) ^ (r_local & 7)) << 4),
@@ -738,7 +753,7 @@ template <int D>
 __global__ void __launch_bounds__(256, 2)
     fwd_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                          float *__restrict__ lse, int n, int n_qblocks, int n_items,
+                          float *__restrict__ lse, float *__restrict__ o32, int n, int n_qblocks, int n_items,
                           float scale_log2, int v_f16, int *status)
 {
     using C = PersistCfg<D>;
@@ -1031,6 +1046,7 @@ __global__ void __launch_bounds__(256, 2)
                 for (int i = 0; i < 16; ++i)
                     pk[i] = ptx::pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l,
                                              __uint_as_float(ov[2 * i + 1]) * inv_l);
+                if (o32 && row < n) store_o32(o32 + ((size_t)bh * n + row) * D + c, ov, inv_l);
                 // columns [c, c + 32) of a 64-column box: chunks (c % 64) / 8 + v4
 #pragma unroll
                 for (int v4 = 0; v4 < 4; ++v4) {
@@ -1067,7 +1083,7 @@ cudaError_t launch_fwd_persistent(const FwdArgs &a, cudaStream_t stream)
     // Two CTAs per SM: TMEM (256 columns each), shared memory and registers are sized for it.
     const long long ctas = std::min<long long>(items, 2LL * device_sm_count());
     fwd_persistent_kernel<D><<<(unsigned)ctas, C::THREADS, C::SMEM_BYTES, stream>>>(
-        a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.lse, a.n, n_qblocks,
+        a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.lse, a.o32, a.n, n_qblocks,
         (int)items, a.scale * kLog2e, a.v_f16, a.status);
     return cudaGetLastError();
 }
@@ -1083,7 +1099,7 @@ cudaError_t launch_fwd_d(const FwdArgs &a, cudaStream_t stream)
     const int n_qblocks = (a.n + rows_per_cta - 1) / rows_per_cta;
     const long long ctas = (long long)n_qblocks * a.bh;
     fwd_kernel<D, NQ><<<(unsigned)ctas, C::THREADS, C::SMEM_BYTES, stream>>>(
-        a.tm_q, a.tm_k, a.tm_v, reinterpret_cast<__nv_bfloat16 *>(a.o), a.lse, a.n, n_qblocks,
+        a.tm_q, a.tm_k, a.tm_v, reinterpret_cast<__nv_bfloat16 *>(a.o), a.lse, a.o32, a.n, n_qblocks,
         a.scale * kLog2e, a.v_f16, a.status);
     return cudaGetLastError();
 }
@@ -1097,7 +1113,7 @@ cudaError_t launch_fwd_sp(const FwdArgs &a, cudaStream_t stream)
     const int n_qblocks = (a.n + C::BM - 1) / C::BM;
     const long long ctas = (long long)n_qblocks * a.bh;
     fwd_sp_kernel<<<(unsigned)ctas, C::THREADS, C::SMEM_BYTES, stream>>>(
-        a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.lse, a.n, n_qblocks, a.scale * kLog2e, a.v_f16, a.status);
+        a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.lse, a.o32, a.n, n_qblocks, a.scale * kLog2e, a.v_f16, a.status);
     return cudaGetLastError();
 }
 

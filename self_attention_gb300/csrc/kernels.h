@@ -17,6 +17,7 @@ struct FwdArgs {
     int bh, n, d;
     float scale;
     int v_f16;                      // 1: tm_v maps an fp16 copy of V (no rewrite in shared memory)
+    float *o32;                     // null, or [BH, N, d] fp32: O before its bf16 rounding (diagnostic)
     int *status;                    // device status word
 };
 

@@ -48,6 +48,20 @@ def o_bound(ref, a_abs):
                       + 2.0 ** -14)
 
 
+def o32_bound(a_abs, qk_abs_max, d: int, scale: float):
+    """Element-wise bound on |O32 - O_ref| for O before its bf16 rounding (attn_fwd_diagnostic):
+    the kernel's own error without the output rounding.  Terms: the weights rounded to fp16
+    (2^-11 A), fp32 accumulation and normalisation (2^-12 A), the scores' fp32 sums of d
+    products, each off by at most gamma_d * scale * sum_c |q_c k_jc| <= gamma_d * scale *
+    qk_abs_max (gamma_d = d u / (1 - d u), u = 2^-24), which move the normalised weights by at
+    most twice that relatively, and fp16's subnormal floor (2^-14).  qk_abs_max is per row
+    (max over keys of sum_c |q_c k_jc|); a_abs = sum_j P_ij |V_j| per element."""
+    u = 2.0 ** -24
+    gamma = d * u / (1 - d * u)
+    ds = gamma * scale * np.asarray(qk_abs_max, np.float64)[..., None]
+    return (2.0 ** -11 + 2.0 ** -12 + 2.0 * ds) * np.asarray(a_abs, np.float64) + 2.0 ** -14
+
+
 # Below this |O| half a bf16 spacing is at most 2^-7, which leaves the kernel's own error room
 # under the stated 1e-2; the workload tests hold every element there to 1e-2 itself.
 O_STRICT_BELOW = 4.0

@@ -109,6 +109,20 @@ def test_fwd_workspace_size_and_argument_errors(lib):
     assert fwd(ws=0, nbytes=0, N=64, d=128, o=Q + 8) == 3
 
 
+def test_fwd_diagnostic_argument_errors(lib):
+    o32 = 0x70000000
+
+    def fwd(o32=o32, o=O, d=64):
+        return lib.attn_fwd_diagnostic(Q, K, V, o, L, o32, 1, 2, 64, d, ctypes.c_float(0.125), None)
+
+    assert fwd(d=96) == 2
+    assert fwd(o32=0) == 1
+    assert fwd(o32=o32 + 4) == 3
+    assert fwd(o32=Q) == 1                # over an input
+    assert fwd(o32=O + 64) == 1           # over the bf16 output
+    assert fwd(o=Q) == 1
+
+
 def test_bwd_argument_errors(lib):
     ws = 0x70000000
     need = sa.attn_bwd_workspace_size(1, 2, 64, 64)
