@@ -427,9 +427,9 @@ struct FwdSpCfg {
     static constexpr int SMEM_BYTES = Q_BYTES + 2 * STAGES * KV_BYTES + 1024;
     static constexpr int THREADS = 256;
     static constexpr int TMA_WARP = 4, MMA_WARP = 5, CONV_WARP = 6, CONV_THREADS = 64;
-    static constexpr int CONV_PASS = 8;   // 8 loads in flight per thread within 88 registers
-    // two CTAs per SM launch with 128 registers a thread: softmax warpgroup 168, the other 88
-    static constexpr uint32_t REG_SOFTMAX = 168, REG_OTHER = 88;
+    static constexpr int CONV_PASS = 8;   // 8 loads in flight per thread within 80 registers
+    // two CTAs per SM launch with 128 registers a thread: softmax warpgroup 176, the other 80
+    static constexpr uint32_t REG_SOFTMAX = 176, REG_OTHER = 80;
     static constexpr uint32_t TM_O = 128, TM_P = 192, TM_COLS = 256;
 };
 
@@ -740,11 +740,11 @@ struct PersistCfg {
     static constexpr int SMEM_BYTES = 2 * Q_BYTES + 2 * STAGES * KV_BYTES + 1024;
     static constexpr int THREADS = 256;
     static constexpr int TMA_WARP = 4, MMA_WARP = 5, CONV_WARP = 6, CONV_THREADS = 64;
-    static constexpr int CONV_PASS = 8;   // 8 loads in flight per thread within 88 registers
-    // two CTAs per SM launch with 128 registers a thread; the softmax warpgroup takes 168 of
-    // them, the producer / issuer / converter warpgroup gives back to 88 (128 x 168 + 128 x 88
-    // = 256 x 128)
-    static constexpr uint32_t REG_SOFTMAX = 168, REG_OTHER = 88;
+    static constexpr int CONV_PASS = 8;   // 8 loads in flight per thread within 80 registers
+    // two CTAs per SM launch with 128 registers a thread; the softmax warpgroup takes 176 of
+    // them (its code spills at 168), the producer / issuer / converter warpgroup gives back to
+    // 80 (128 x 176 + 128 x 80 = 256 x 128)
+    static constexpr uint32_t REG_SOFTMAX = 176, REG_OTHER = 80;
     static constexpr uint32_t TM_O = 128, TM_P = 128 + D;
     static constexpr uint32_t TM_COLS = 128 + D + 64 <= 256 ? 256 : 512;
 };
