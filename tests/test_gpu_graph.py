@@ -21,8 +21,9 @@ def _lib():
     sa.load_library(build())
 
 
-@pytest.mark.parametrize("shape", [(4, 12, 196, 64), (1, 4, 1000, 128)])
+@pytest.mark.parametrize("shape", [(4, 12, 196, 64), (1, 4, 1000, 128), (1, 96, 200, 64)])
 def test_graph_replay_matches_eager(shape):
+    """The last shape takes the whole-head backward (d_k = 64, N <= 256, one head per CTA)."""
     B, H, N, D = shape
     scale = 1.0 / math.sqrt(D)
     dev = lambda t: t.cuda()
@@ -114,3 +115,45 @@ def test_graph_replay_deterministic_bitwise(shape):
     torch.cuda.synchronize()
     for name, a, b in zip(("o", "lse", "dq", "dk", "dv"), replay, (t.float().cpu().numpy() for t in eager_outs)):
         np.testing.assert_array_equal(a, b, err_msg=name)
+
+
+@pytest.mark.parametrize("shape", [(1, 4, 2048, 64), (1, 2, 8192, 128)])
+def test_graph_replay_forward_with_workspace(shape):
+    """attn_fwd_with_workspace (V rounded to fp16 into the workspace, then the forward kernel)
+    captured once with fixed buffers and replayed on new inputs: O and LSE equal eager forward()
+    bit for bit."""
+    B, H, N, D = shape
+    scale = 1.0 / math.sqrt(D)
+    fwsb = sa.attn_fwd_workspace_size(B, H, N, D)
+    assert fwsb > 0
+    fws = torch.empty(fwsb, dtype=torch.uint8, device="cuda")
+    bufs = {x: torch.empty(B, H, N, D, dtype=torch.bfloat16, device="cuda") for x in ("q", "k", "v")}
+    o = torch.empty(B, H, N, D, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(B, H, N, device="cuda")
+    s = torch.cuda.Stream()
+
+    def step():
+        sa.attn_fwd_with_workspace(bufs["q"], bufs["k"], bufs["v"], o, lse, fws, fwsb, B, H, N, D, scale, s)
+
+    first = make_qkv(B, H, N, D, seed=9600 + N, with_do=False)
+    for x in bufs:
+        bufs[x].copy_(first[x])
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step()
+    torch.cuda.synchronize()
+    for seed in (9700 + N, 9800 + N):
+        inp = make_qkv(B, H, N, D, seed=seed, with_do=False)
+        for x in bufs:
+            bufs[x].copy_(inp[x])
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert sa.attn_get_device_status() == 0
+        ref_o, ref_lse = sa.forward(*(inp[x].cuda() for x in ("q", "k", "v")), scale)
+        assert torch.equal(o, ref_o)
+        assert torch.equal(lse, ref_lse)
