@@ -29,6 +29,12 @@
 //   3. convert: dQ = bf16(scale * accumulator).
 // TMEM columns: dK [0,d), dV [d,2d), then two buffers of {S^T/P^T/dQ^T (64), dP^T (64)}.
 // dQ^T has M = d rows; for d = 64 the MMA still runs with M = 128 and lanes 64-127 are unused.
+//
+// Further in this file: the d = 64 main kernels with 128-query tiles (one CTA per key block,
+// and a persistent one over (head, key block) items), the deterministic mode's dK / dV pass for
+// d = 128 and its query-stationary dQ pass, and, for short d = 64 sequences over few heads, a
+// kernel that takes each head whole (statistics, all products and dQ, dK, dV in one launch,
+// dQ accumulated in TMEM).
 #include "common.cuh"
 #include "kernels.h"
 
