@@ -163,9 +163,10 @@ def test_fwd_deterministic():
     np.testing.assert_array_equal(a[1], b[1])
 
 
-def test_fwd_invariants_on_gpu():
+@pytest.mark.parametrize("d", [64, 128])
+def test_fwd_invariants_on_gpu(d):
     """Q = 0 gives mean(V) and LSE = log N; permuting K/V rows jointly leaves O unchanged."""
-    inp = make_qkv(1, 2, 300, 64, seed=3, with_do=False)
+    inp = make_qkv(1, 2, 300, d, seed=3, with_do=False)
     z = dict(inp, q=torch.zeros_like(inp["q"]))
     o, lse = run_fwd(z, 0.125)
     mean_v = inp["v"].double().mean(dim=2, keepdim=True).expand_as(inp["v"]).numpy()
@@ -178,6 +179,35 @@ def test_fwd_invariants_on_gpu():
     o2, l2 = run_fwd(p, 0.125)
     np.testing.assert_allclose(o2, o1, rtol=0, atol=2 ** -7)
     np.testing.assert_allclose(l2, l1, rtol=0, atol=1e-5)
+
+
+@pytest.mark.parametrize("d,h,n", [(64, 3, 700), (64, 64, 700), (128, 3, 700), (64, 3, 5000)])
+def test_fwd_dominant_key_on_gpu(d, h, n):
+    """One dominant key per row: with K = alpha Q (alpha 64 at d = 64, 16 at d = 128, powers of
+    two so K stays exact), query i's own key leads every other logit by more than 40, so its
+    weight is 1 to within e^-40 and O_i = V_i, LSE_i = S_ii (the definition in the limit).  The
+    rows' dominant keys sit in every key tile, so the running maximum jumps by far more than
+    kTau across tiles.  The largest weight is 2^kPOff to within the rounding of the maximum, so
+    O comes back as V: bitwise where V is in fp16's normal range, and within fp16's subnormal
+    step (2^-24, V meets P on fp16 tensor cores) below it.  (64, 64, 700) has enough query
+    tiles for the persistent d = 64 kernel; the others run the one-tile-per-CTA kernels."""
+    alpha = 64 if d == 64 else 16
+    inp = make_qkv(1, h, n, d, seed=31, with_do=False)
+    q = inp["q"]
+    inp = dict(inp, k=(q.float() * alpha).bfloat16())
+    scale = 1.0 / math.sqrt(d)
+    o, lse = run_fwd(inp, scale)
+    qd = q.double()
+    s_ii = (qd * (qd * alpha)).sum(-1).numpy() * scale
+    others = torch.einsum("bhid,bhjd->bhij", qd, qd * alpha) * scale
+    others.diagonal(dim1=-2, dim2=-1).fill_(-float("inf"))
+    gap = s_ii - others.amax(-1).numpy()
+    assert gap.min() > 40, gap.min()
+    v = inp["v"].float().numpy()
+    normal = np.abs(v) >= 2.0 ** -14
+    np.testing.assert_array_equal(o[normal], v[normal])
+    np.testing.assert_allclose(o[~normal], v[~normal], rtol=0, atol=2.0 ** -24)
+    np.testing.assert_allclose(lse, s_ii, rtol=1e-6, atol=0)
 
 
 def _sampled_check(w, inp, o, lse, heads, rows_per_head, seed):
