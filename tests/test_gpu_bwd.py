@@ -35,7 +35,7 @@ def _intact(buf):
     return bool(torch.isnan(torch.cat([buf[:GUARD], buf[-GUARD:]])).all())
 
 
-def run_fwd_bwd(inp, scale):
+def run_fwd_bwd(inp, scale, deterministic=False):
     q, k, v, do = (inp[x].cuda() for x in ("q", "k", "v", "do"))
     B, H, N, D = q.shape
     o, lse = sa.forward(q, k, v, scale)
@@ -43,7 +43,8 @@ def run_fwd_bwd(inp, scale):
     dq, dk, dv = (b[1] for b in bufs)
     ws_bytes = sa.attn_bwd_workspace_size(B, H, N, D)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
-    sa.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, ws_bytes, B, H, N, D, scale)
+    call = sa.attn_bwd_deterministic if deterministic else sa.attn_bwd
+    call(q, k, v, o, do, lse, dq, dk, dv, ws, ws_bytes, B, H, N, D, scale)
     assert sa.attn_get_device_status() == 0
     assert all(_intact(b[0]) for b in bufs), "a store escaped a gradient tensor"
     to = lambda t: t.float().cpu().numpy()
@@ -127,15 +128,26 @@ def test_bwd_wide_logits_and_scale(d):
             check_grad(name, got[name], ref[name], f"d={d} scale={scale}")
 
 
-def test_bwd_identities_on_gpu():
-    """sum_j dK_j = 0 and sum_j dV_j = sum_i dO_i hold for the GPU gradients too."""
-    inp = make_qkv(2, 3, 517, 128, seed=22)
-    got = run_fwd_bwd(inp, 1.0 / math.sqrt(128))
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("deterministic", [False, True])
+def test_bwd_identities_on_gpu(d, deterministic):
+    """sum_j dK_j = 0 and sum_j dV_j = sum_i dO_i hold for the GPU gradients too.  And moving
+    every key by one vector w adds scale q_i . w to a whole row of logits, which moves no weight:
+    dV = P^T dO and dK = scale dS^T Q stay, and so does dQ = scale dS K, since every row of dS
+    sums to 0 (up to the bf16 rounding of the shifted keys)."""
+    inp = make_qkv(2, 3, 517, d, seed=22)
+    scale = 1.0 / math.sqrt(d)
+    got = run_fwd_bwd(inp, scale, deterministic)
     dk_sum = got["dk"].sum(axis=2)
     assert np.abs(dk_sum).max() <= 2e-2 * np.abs(got["dk"]).max() * math.sqrt(517)
     dv_sum = got["dv"].sum(axis=2)
     do_sum = inp["do"].double().sum(dim=2).numpy()
     assert np.abs(dv_sum - do_sum).max() <= 1e-2 * max(np.abs(do_sum).max(), 1.0)
+    w = torch.linspace(-1.0, 1.0, d)
+    shifted = dict(inp, k=(inp["k"].float() + w).bfloat16())
+    got2 = run_fwd_bwd(shifted, scale, deterministic)
+    for name in ("dq", "dk", "dv"):
+        check_grad(f"{name} (key shift)", got2[name], got[name].astype(np.float64), f"d={d}")
 
 
 def test_bwd_dk_dv_deterministic():
